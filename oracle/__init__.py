@@ -1,0 +1,316 @@
+"""FP64 CPU oracle for the DeepSeekMoE layer forward (test infrastructure).
+
+Only the tests, the package's smoke check and the benchmark's CPU-baseline
+leg may import this package. It wraps the plain C file `moe_oracle.c`
+(compiled here with gcc, no fast-math, no FP contraction) through ctypes and
+composes its pieces into the layer. It shares no code with the CUDA library
+and never imports it.
+
+Parity pins: every function here is checked in tests/test_oracle_*.py
+against something other than itself (closed forms, brute force with numpy,
+torch's float8_e4m3fn conversion, invariants). The layer value at the full
+V3 shape has no printed worked example to compare with; it is pinned only
+through its stages.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+          "-fPIC", "-shared", "-Wall"]
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into liboracle.so (next to it) if stale."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _P(t):
+    return ctypes.POINTER(t)
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
+            i64, i32, dbl, flt = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_float
+            vp = ctypes.c_void_p
+            sig = {
+                "oracle_threads": (i32, []),
+                "oracle_init": (None, []),
+                "oracle_bf16_value": (dbl, [ctypes.c_uint16]),
+                "oracle_bf16_round": (ctypes.c_uint16, [dbl]),
+                "oracle_e4m3_value": (dbl, [ctypes.c_uint8]),
+                "oracle_e4m3_encode": (ctypes.c_uint8, [flt]),
+                "oracle_e4m3_boundary_distance": (dbl, [flt]),
+                "oracle_bf16_round_array": (None, [vp, i64, vp]),
+                "oracle_e4m3_encode_array": (None, [vp, i64, vp]),
+                "oracle_quant_1x128": (None, [vp, i64, i64, vp, vp]),
+                "oracle_quant_1x128_f32": (None, [vp, i64, i64, vp, vp]),
+                "oracle_quant_128x128": (None, [vp, i64, i64, vp, vp]),
+                "oracle_route": (None, [vp, i64, i64, vp, vp, vp, i32, i32, i32, i32, dbl,
+                                        vp, vp, vp, vp, vp, vp]),
+                "oracle_permute": (None, [vp, i64, i32, i32, vp, vp, vp]),
+                "oracle_fp8_gemm": (None, [vp, vp, vp, vp, i64, i64, i64, vp]),
+                "oracle_bf16_gemm": (None, [vp, vp, i64, i64, i64, vp]),
+                "oracle_swiglu": (None, [vp, vp, i64, vp]),
+                "oracle_swiglu_quant": (None, [vp, vp, i64, i64, vp, vp, vp, vp]),
+                "oracle_combine": (None, [vp, vp, vp, vp, vp, i64, i64, i32, vp]),
+                "oracle_bias_update": (None, [vp, vp, i32, i64, i32, flt]),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            L.oracle_init()
+            _lib = L
+        return _lib
+
+
+def threads() -> int:
+    return int(lib().oracle_threads())
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def as_bf16_bits(x) -> np.ndarray:
+    """uint16 bit patterns of a bf16 torch tensor (or pass uint16 through)."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch
+    return x.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+# --------------------------------------------------------------------------
+# formats
+# --------------------------------------------------------------------------
+
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """uint16 bf16 bits of x rounded once, to nearest even, from FP64."""
+    flat = _c(np.asarray(x, dtype=np.float64).ravel(), np.float64)
+    out = np.empty(flat.size, np.uint16)
+    lib().oracle_bf16_round_array(_ptr(flat), flat.size, _ptr(out))
+    return out.reshape(np.shape(x))
+
+
+def e4m3_values() -> np.ndarray:
+    """The 256 code values (NaN for 0x7F / 0xFF)."""
+    L = lib()
+    return np.array([L.oracle_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(v: np.ndarray) -> np.ndarray:
+    """E4M3 codes of fp32 values (nearest, ties to even, saturating)."""
+    flat = _c(np.asarray(v, dtype=np.float32).ravel(), np.float32)
+    out = np.empty(flat.size, np.uint8)
+    lib().oracle_e4m3_encode_array(_ptr(flat), flat.size, _ptr(out))
+    return out.reshape(np.shape(v))
+
+
+# --------------------------------------------------------------------------
+# quantisation
+# --------------------------------------------------------------------------
+
+def quant_1x128(x_bf16) -> tuple[np.ndarray, np.ndarray]:
+    """(q uint8 [R,C], scales fp32 [R, C/128]) from bf16 [R,C]."""
+    x = as_bf16_bits(x_bf16)
+    R, C = x.shape
+    assert C % 128 == 0
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R, C // 128), np.float32)
+    lib().oracle_quant_1x128(_ptr(x), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_1x128_f32(x: np.ndarray):
+    x = _c(x, np.float32)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty((R, C // 128), np.float32)
+    lib().oracle_quant_1x128_f32(_ptr(x), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_128x128(w_bf16) -> tuple[np.ndarray, np.ndarray]:
+    """(q uint8 [R,C], scales fp32 [ceil(R/128), C/128]) from bf16 [R,C]."""
+    w = as_bf16_bits(w_bf16)
+    R, C = w.shape
+    assert C % 128 == 0
+    q = np.empty((R, C), np.uint8)
+    s = np.empty(((R + 127) // 128, C // 128), np.float32)
+    lib().oracle_quant_128x128(_ptr(w), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+# --------------------------------------------------------------------------
+# routing, permutation, bias
+# --------------------------------------------------------------------------
+
+class Route:
+    def __init__(self, topk_idx, gates, scores, key_gap, loads, near_tie):
+        self.topk_idx, self.gates, self.scores = topk_idx, gates, scores
+        self.key_gap, self.loads, self.near_tie = key_gap, loads, near_tie
+
+
+def route(u_bf16, centroids, bias: np.ndarray, K: int, n_groups: int = 1, topk_groups: int = 1,
+          delta: float = 0.0, want_scores: bool = False) -> Route:
+    """Sigmoid affinities, biased top-K (optionally group-limited), gates, loads.
+
+    centroids: fp32 numpy/torch array, or a bf16 torch tensor / uint16 array.
+    """
+    u = as_bf16_bits(u_bf16)
+    T, d = u.shape
+    cf = cb = None
+    import torch
+    if isinstance(centroids, torch.Tensor) and centroids.dtype == torch.bfloat16:
+        cb = as_bf16_bits(centroids)
+    elif isinstance(centroids, np.ndarray) and centroids.dtype == np.uint16:
+        cb = centroids
+    else:
+        cf = _c(centroids.cpu().numpy() if isinstance(centroids, torch.Tensor) else centroids, np.float32)
+    N = (cf if cf is not None else cb).shape[0]
+    b = _c(bias.cpu().numpy() if isinstance(bias, torch.Tensor) else bias, np.float32)
+    idx = np.empty((T, K), np.int32)
+    g = np.empty((T, K), np.float64)
+    s = np.empty((T, N), np.float64) if want_scores else None
+    gap = np.empty(T, np.float64)
+    loads = np.empty(N, np.int32)
+    near = np.empty(T, np.int32)
+    lib().oracle_route(_ptr(u), T, d, _ptr(cf), _ptr(cb), _ptr(b), N, K, n_groups, topk_groups,
+                       float(delta), _ptr(idx), _ptr(g), _ptr(s), _ptr(gap), _ptr(loads), _ptr(near))
+    return Route(idx, g, s, gap, loads, near.astype(bool))
+
+
+def permute(topk_idx: np.ndarray, N: int):
+    """(offsets [N+1], perm_token [T*K], dest_row [T,K]) by stable counting sort."""
+    idx = _c(topk_idx, np.int32)
+    T, K = idx.shape
+    off = np.empty(N + 1, np.int32)
+    perm = np.empty(T * K, np.int32)
+    dest = np.empty((T, K), np.int32)
+    lib().oracle_permute(_ptr(idx), T, N, K, _ptr(off), _ptr(perm), _ptr(dest))
+    return off, perm, dest
+
+
+def bias_update(bias: np.ndarray, loads: np.ndarray, T: int, K: int, gamma: float) -> np.ndarray:
+    b = _c(bias, np.float32).copy()
+    ld = _c(loads, np.int32)
+    lib().oracle_bias_update(_ptr(b), _ptr(ld), b.size, T, K, float(np.float32(gamma)))
+    return b
+
+
+# --------------------------------------------------------------------------
+# GEMMs, activation, combine
+# --------------------------------------------------------------------------
+
+def fp8_gemm(qa, sa, qb, sb) -> np.ndarray:
+    """FP64 C [M,Nd] of the block-scaled FP8 product (see moe_oracle.c)."""
+    qa, qb = _c(qa, np.uint8), _c(qb, np.uint8)
+    sa, sb = _c(sa, np.float32), _c(sb, np.float32)
+    M, Kd = qa.shape
+    Nd = qb.shape[0]
+    C = np.empty((M, Nd), np.float64)
+    lib().oracle_fp8_gemm(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, Nd, Kd, _ptr(C))
+    return C
+
+
+def bf16_gemm(a_bf16, b_bf16) -> np.ndarray:
+    a, b = as_bf16_bits(a_bf16), as_bf16_bits(b_bf16)
+    M, Kd = a.shape
+    Nd = b.shape[0]
+    C = np.empty((M, Nd), np.float64)
+    lib().oracle_bf16_gemm(_ptr(a), _ptr(b), M, Nd, Kd, _ptr(C))
+    return C
+
+
+def swiglu(h1: np.ndarray, h3: np.ndarray) -> np.ndarray:
+    h1, h3 = _c(h1, np.float64), _c(h3, np.float64)
+    a = np.empty_like(h1)
+    lib().oracle_swiglu(_ptr(h1), _ptr(h3), h1.size, _ptr(a))
+    return a
+
+
+def swiglu_quant(h1: np.ndarray, h3: np.ndarray):
+    """(q [R,I], scales [R,I/128], boundary distance [R,I], a/scale [R,I])."""
+    h1, h3 = _c(h1, np.float64), _c(h3, np.float64)
+    R, I = h1.shape
+    q = np.empty((R, I), np.uint8)
+    s = np.empty((R, I // 128), np.float32)
+    dist = np.empty((R, I), np.float64)
+    v = np.empty((R, I), np.float64)
+    lib().oracle_swiglu_quant(_ptr(h1), _ptr(h3), R, I, _ptr(q), _ptr(s), _ptr(dist), _ptr(v))
+    return q, s, dist, v
+
+
+def combine(u_bf16, y_shared_bf16, y_bf16, gates: np.ndarray, dest_row: np.ndarray) -> np.ndarray:
+    u = as_bf16_bits(u_bf16)
+    ys = None if y_shared_bf16 is None else as_bf16_bits(y_shared_bf16)
+    y = as_bf16_bits(y_bf16)
+    g = _c(gates, np.float64)
+    dr = _c(dest_row, np.int32)
+    T, d = u.shape
+    K = g.shape[1]
+    out = np.empty((T, d), np.float64)
+    lib().oracle_combine(_ptr(u), _ptr(ys), _ptr(y), _ptr(g), _ptr(dr), T, d, K, _ptr(out))
+    return out
+
+
+# --------------------------------------------------------------------------
+# the layer, composed from the pieces above
+# --------------------------------------------------------------------------
+
+def expert_ffn_fp8(xq, xs, w1, w3, w2, want_detail: bool = False):
+    """One SwiGLU expert on FP8 rows: y = W2 (silu(W1 x) * W3 x).
+
+    xq/xs: the rows' E4M3 codes [R,d] and 1x128 scales [R,d/128];
+    w1, w3 [I,d] and w2 [d,I] bf16 weights, quantised here per 128x128 block.
+    The intermediate is re-quantised per 1x128 tile; y is FP64 [R,d].
+    """
+    q1, s1 = quant_128x128(w1)
+    q3, s3 = quant_128x128(w3)
+    q2, s2 = quant_128x128(w2)
+    h1 = fp8_gemm(xq, xs, q1, s1)
+    h3 = fp8_gemm(xq, xs, q3, s3)
+    aq, as_, dist, v = swiglu_quant(h1, h3)
+    y = fp8_gemm(aq, as_, q2, s2)
+    if want_detail:
+        return y, dict(aq=aq, as_=as_, dist=dist, v=v, q2=q2, s2=s2)
+    return y
+
+
+def expert_ffn_bf16(x_bf16, w1, w3, w2):
+    """One SwiGLU expert in bf16 with exact products: h = x W^T in FP64,
+    a = silu(h1) * h3 rounded to bf16 (where the bf16 path stores it),
+    y = a W2^T in FP64."""
+    h1 = bf16_gemm(x_bf16, w1)
+    h3 = bf16_gemm(x_bf16, w3)
+    a = bf16_round(swiglu(h1, h3))
+    return bf16_gemm(a, w2)
