@@ -1,0 +1,236 @@
+/*
+ * moe.h — C ABI of the B300 (sm_103a) DeepSeekMoE layer forward.
+ *
+ * What the layer computes (DeepSeek-V3 Technical Report, as summarised on
+ * learn.ifs.name "DeepSeek-V3 Technical Report" and nlp-lineage.vercel.app
+ * "DeepSeek-V3 Technical Report (2024)"):
+ *
+ *   s_{i,t} = sigmoid(u_t . e_i)          affinity of token t to expert i's centroid
+ *   chosen  = top-K of s_{i,t} + b_i       the bias b_i steers the choice only
+ *   g_{i,t} = s_{i,t} / sum_chosen s       gates normalised over the chosen experts
+ *   h'_t    = u_t + FFN_shared(u_t) + sum_chosen g_{i,t} FFN_i(u_t)
+ *   after the step: b_i -= gamma if expert i was overloaded, += gamma if underloaded
+ *
+ * with every expert FFN a SwiGLU MLP run as FP8 GEMMs: activations scaled per
+ * 1x128 tile, weights per 128x128 block, partial sums promoted to FP32 every
+ * 128 K-elements where the two scales are applied.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE memory owned by the caller, except in
+ *     moe_layer_forward_host, whose u/out are host memory. The library never
+ *     allocates or frees device memory; scratch comes from a caller workspace
+ *     sized by the matching *_workspace_size function.
+ *   - Calls are asynchronous on `stream` and return synchronously checked
+ *     argument errors. Device-side problems (a pipeline wait that ran out of
+ *     time, inconsistent group offsets) set a device status word that
+ *     moe_get_device_status() reads.
+ *   - bf16 is passed as uint16_t bit patterns, OCP FP8 E4M3 as uint8_t,
+ *     scales as fp32. Row-major unless stated.
+ *   - Activation scales are stored K-block-major: scales[kb * ld + row]
+ *     (kb = column / 128). Weight scales are [rows/128][cols/128] row-major.
+ *   - Pointers used by vector or TMA loads must be 16-byte aligned.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size           */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement   */
+    MOE_ERR_CUDA = 3,          /* a CUDA runtime call failed                 */
+    MOE_ERR_TIMEOUT = 4,       /* device: a bounded pipeline wait gave up    */
+    MOE_ERR_WORKSPACE = 5,     /* workspace missing or too small            */
+    MOE_ERR_DEVICE_DATA = 6    /* device: offsets/indices out of range       */
+} moe_status;
+
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1, MOE_DTYPE_E4M3 = 2 };
+
+enum {
+    MOE_EPI_BF16 = 0,          /* C = bf16(A B^T)                                         */
+    MOE_EPI_SWIGLU_FP8 = 1,    /* C = e4m3 1x128 quant of silu(h_gate) * h_up, + scales   */
+    MOE_EPI_SWIGLU_BF16 = 2,   /* C = bf16(silu(h_gate) * h_up)                           */
+    MOE_EPI_F32 = 3            /* C = fp32(A B^T)                                         */
+};
+
+/* Human-readable text of the last host-side error (thread-local). */
+const char* moe_last_error(void);
+
+/* Number of SMs the kernels size their persistent grids for (device 0 at first call). */
+int moe_num_sms(void);
+
+/*
+ * Device status word: synchronises `stream`, returns the worst status any
+ * kernel recorded since the last call (MOE_OK if none) and clears it.
+ */
+moe_status moe_get_device_status(moe_stream_t stream, int* status);
+
+/* ------------------------------------------------------------------------ */
+/* FP8 quantisation — learn.ifs.name summary, paragraph on FP8 scaling:      */
+/* one scale per 1x128 activation tile and per 128x128 weight block, so an   */
+/* outlier only affects its own group. scale = amax/448 (1 for an all-zero    */
+/* tile), q = e4m3_rn_satfinite(x / scale), both divisions IEEE fp32.         */
+/* ------------------------------------------------------------------------ */
+
+/* x bf16 [rows, cols] (row stride ld_x elements), cols % 128 == 0.
+ * q e4m3 [rows, cols] (row stride cols); scales[kb * ld_s + r], ld_s >= rows. */
+moe_status fp8_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x,
+                           uint8_t* q, float* scales, int64_t ld_s, moe_stream_t stream);
+
+/* w bf16 [rows, cols], cols % 128 == 0 (a last partial row block holds the
+ * rows that exist). q e4m3 [rows, cols]; scales [ceil(rows/128)][cols/128]. */
+moe_status fp8_quant_128x128(const uint16_t* w, int64_t rows, int64_t cols,
+                             uint8_t* q, float* scales, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Routing — learn.ifs.name summary, MoE and bias paragraphs; nlp-lineage    */
+/* page, "The notation": chosen iff s + b is among the top K; the bias       */
+/* affects only the choice. Ties go to the lower expert index.               */
+/* ------------------------------------------------------------------------ */
+
+/* u bf16 [T, d]; centroids [N, d] bf16 or fp32 (centroid_dtype); bias fp32 [N].
+ * n_groups = 1: flat top-K. n_groups > 1: experts form n_groups groups of
+ * N/n_groups consecutive ids, a group's score is the sum of its two largest
+ * s + b, and only the topk_groups best groups (ties: lower group) compete.
+ * Outputs: topk_idx int32 [T, K] (ascending expert id per token), gates fp32
+ * [T, K] (s / sum s over the chosen), loads int32 [N] (overwritten: tokens
+ * per expert), scores fp32 [T, N] (s; may be NULL).
+ * Limits: d % 64 == 0, 1 <= K <= 16, K <= N <= 1024, N % 16 == 0 when
+ * centroids are fp32 (tensor-core gate), n_groups <= 32. */
+size_t moe_route_workspace_size(int64_t T, int d, int N, int centroid_dtype);
+moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype,
+                     const float* bias, int N, int K, int n_groups, int topk_groups,
+                     int32_t* topk_idx, float* gates, int32_t* loads, float* scores,
+                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Permutation — the single-GPU form of the dispatch step (learn.ifs.name    */
+/* summary, paragraph on all-to-all dispatch/combine): a stable counting     */
+/* sort of the (token, expert) pairs by expert, tokens ascending within one  */
+/* expert, no pair dropped (nlp-lineage page, load-balancing item).          */
+/* ------------------------------------------------------------------------ */
+
+/* x bf16 [T, d]; topk_idx int32 [T, K] with entries in [0, N).
+ * out_dtype MOE_DTYPE_BF16: x_perm bf16 rows; MOE_DTYPE_E4M3: x_perm e4m3
+ * rows quantised per 1x128 tile, scales[kb * R + row] with R the row count.
+ * with_shared != 0 appends rows T*K .. T*K+T-1 = x[0..T-1] (the shared
+ * expert's group), so R = T*K + T and offsets has N + 2 entries; else
+ * R = T*K and offsets has N + 1 entries (offsets[i] = first row of expert i).
+ * perm_token int32 [T*K]: source token of each routed row;
+ * dest_row int32 [T, K]: row of each (token, k). d % 128 == 0. */
+size_t moe_permute_workspace_size(int64_t T, int N);
+moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K,
+                       int out_dtype, int with_shared, int32_t* offsets, int32_t* perm_token,
+                       int32_t* dest_row, void* x_perm, float* x_perm_scales,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped GEMMs — learn.ifs.name summary, paragraphs on FP8 tiles and on     */
+/* promotion: every 128 K-elements the partial sums go to FP32 and the       */
+/* per-group scales are applied there.                                       */
+/* ------------------------------------------------------------------------ */
+
+/* For each group g (rows group_offsets[g] .. group_offsets[g+1]-1 of A):
+ *   C[rows] = epilogue( sum_kb sa[kb][row] * sb[g][n/128][kb] * (A[row, kb] . B[g][n, kb]) )
+ * A e4m3 [M_total, Kd]; sa fp32 [Kd/128][M_total]; B e4m3 [G][Nd][Kd] (K
+ * contiguous); sb fp32 [G][Nd/128][Kd/128]; group_offsets int32 [G+1] in
+ * DEVICE memory, non-decreasing from 0 to <= M_total.
+ * MOE_EPI_BF16: C bf16 [M_total, Nd].
+ * MOE_EPI_SWIGLU_FP8: B's rows alternate per 128 between the gate and the up
+ * projection (rows 256j..256j+127 = W1 rows 128j.., rows 256j+128.. = W3 rows
+ * 128j..); C e4m3 [M_total, Nd/2] = 1x128 quant of silu(h1) * h3 with scales
+ * c_scales[j * M_total + row] (j = output column / 128).
+ * Limits: Kd % 128 == 0, Nd % 256 == 0, G <= 1024. Rows past a group's end are
+ * never written. */
+moe_status fp8_grouped_gemm(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                            const int32_t* group_offsets, int G, int64_t M_total, int Nd, int Kd,
+                            int epilogue, void* C, float* c_scales, moe_stream_t stream);
+
+/* Same grouping with bf16 A [M_total, Kd], B [G][Nd][Kd] and FP32
+ * accumulation over the whole K (no scales). epilogue MOE_EPI_BF16 (C bf16
+ * [M_total, Nd]), MOE_EPI_SWIGLU_BF16 (C bf16 [M_total, Nd/2], rows of B
+ * interleaved as above) or MOE_EPI_F32 (C fp32 [M_total, Nd]).
+ * Limits: Kd % 64 == 0, Nd % 256 == 0, G <= 1024. */
+moe_status bf16_grouped_gemm(const uint16_t* A, const uint16_t* B, const int32_t* group_offsets,
+                             int G, int64_t M_total, int Nd, int Kd, int epilogue, void* C,
+                             moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Combine — nlp-lineage page, "The notation":                               */
+/*   h'_t = u_t + y_shared_t + sum_k g_{t,k} y_{dest_row[t,k]}               */
+/* accumulated in fp32 in that order (k ascending), stored as bf16.          */
+/* ------------------------------------------------------------------------ */
+
+/* u bf16 [T, d]; y_shared bf16 [T, d] or NULL; y_perm bf16 [R, d];
+ * gates fp32 [T, K]; dest_row int32 [T, K] in [0, R); out bf16 [T, d].
+ * d % 8 == 0. */
+moe_status moe_combine(const uint16_t* u, const uint16_t* y_shared, const uint16_t* y_perm,
+                       const float* gates, const int32_t* dest_row, int64_t T, int d, int K,
+                       int64_t R, uint16_t* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Bias update — learn.ifs.name summary, bias paragraph; nlp-lineage page,   */
+/* load-balancing item. Overloaded = load above the mean T*K/N (compared as  */
+/* load*N vs T*K): b -= gamma; below: b += gamma; equal: unchanged.          */
+/* ------------------------------------------------------------------------ */
+
+moe_status moe_bias_update(float* bias, const int32_t* loads, int N, int64_t T, int K, float gamma,
+                           moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* The whole layer, composed from the calls above.                           */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int d, N, K, I;            /* hidden, routed experts, experts per token, SwiGLU width   */
+    int n_groups, topk_groups; /* routing groups (1, 1 = flat)                              */
+    float gamma;               /* bias step                                                 */
+    int fp8;                   /* 1: e4m3 weights + scales; 0: bf16 weights, no scales      */
+    const void* centroids;     /* [N, d] */
+    int centroid_dtype;        /* MOE_DTYPE_F32 or MOE_DTYPE_BF16                           */
+    float* bias;               /* [N] fp32, updated in place when update_bias != 0          */
+    const void* w13;           /* [N+1][2I][d], gate/up rows interleaved per 128; expert N = shared */
+    const float* w13_scales;   /* [N+1][2I/128][d/128] (fp8 only)                           */
+    const void* w2;            /* [N+1][d][I]                                               */
+    const float* w2_scales;    /* [N+1][d/128][I/128] (fp8 only)                            */
+} moe_layer_weights;
+
+/* Optional outputs of one forward (any may be NULL except loads). */
+typedef struct {
+    int32_t* topk_idx;         /* [T, K] */
+    float* gates;              /* [T, K] */
+    int32_t* loads;            /* [N], required */
+} moe_layer_outputs;
+
+size_t moe_layer_workspace_size(const moe_layer_weights* w, int64_t T);
+
+/* h' for T tokens: u bf16 [T, d] -> out bf16 [T, d] (device), then the bias
+ * update from this step's loads when update_bias != 0. Launch sequence:
+ * route, permute (with FP8 quantisation of the rows when fp8), grouped GEMM 1
+ * with SwiGLU, grouped GEMM 2, combine, bias update. */
+moe_status moe_layer_forward(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
+                             const moe_layer_outputs* outs, int update_bias,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* As moe_layer_forward with u_host / out_host in HOST memory (pinned for
+ * speed): copies u in, runs the layer, copies h' back, all on `stream`.
+ * The device copies of u and out live in the workspace
+ * (moe_layer_host_workspace_size). */
+size_t moe_layer_host_workspace_size(const moe_layer_weights* w, int64_t T);
+moe_status moe_layer_forward_host(const moe_layer_weights* w, const uint16_t* u_host, int64_t T,
+                                  uint16_t* out_host, const moe_layer_outputs* outs, int update_bias,
+                                  void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,382 @@
+// The C ABI (include/moe.h): argument validation, workspace layout and the
+// launch sequence of the layer. No entry point allocates device memory.
+#include <cstdarg>
+#include <cstdio>
+
+#include "common.cuh"
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+
+int num_sms() {
+    static int n = 0;
+    if (n <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+}  // namespace moe
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+#define REQUIRE(cond, ...)                                    \
+    do {                                                      \
+        if (!(cond)) return fail(MOE_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+#define UNSUPPORTED(cond, ...)                                \
+    do {                                                      \
+        if (!(cond)) return fail(MOE_ERR_UNSUPPORTED, __VA_ARGS__); \
+    } while (0)
+#define CUDA_OK(expr)                                                                              \
+    do {                                                                                           \
+        cudaError_t e_ = (expr);                                                                   \
+        if (e_ != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+    } while (0)
+#define STATUS_OK(expr)                  \
+    do {                                 \
+        moe_status s_ = (expr);          \
+        if (s_ != MOE_OK) return s_;     \
+    } while (0)
+
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+moe_status check_route(const uint16_t* u, int64_t T, int d, const void* centroids, int cdt, const float* bias, int N,
+                       int K, int n_groups, int topk_groups, const int32_t* idx, const float* gates,
+                       const int32_t* loads) {
+    REQUIRE(T >= 0 && T <= kMaxRows, "moe_route: T=%lld out of range", (long long)T);
+    REQUIRE(d > 0 && d % 64 == 0, "moe_route: d=%d must be a positive multiple of 64", d);
+    REQUIRE(K >= 1 && K <= 16 && K <= N, "moe_route: K=%d must satisfy 1 <= K <= min(16, N)", K);
+    REQUIRE(N >= 1 && N <= 1024, "moe_route: N=%d must be in [1, 1024]", N);
+    REQUIRE(cdt == MOE_DTYPE_F32 || cdt == MOE_DTYPE_BF16, "moe_route: centroid dtype %d", cdt);
+    REQUIRE(n_groups >= 1 && n_groups <= 32 && N % n_groups == 0, "moe_route: n_groups=%d must divide N", n_groups);
+    if (n_groups > 1) {
+        REQUIRE(N / n_groups >= 2, "moe_route: groups need at least two experts");
+        REQUIRE(topk_groups >= 1 && topk_groups <= n_groups, "moe_route: topk_groups=%d", topk_groups);
+        REQUIRE(topk_groups * (N / n_groups) >= K, "moe_route: kept groups hold fewer than K experts");
+    }
+    REQUIRE(u && centroids && bias && idx && gates && loads, "moe_route: null pointer");
+    REQUIRE(al16(u) && al16(centroids), "moe_route: u and centroids must be 16-byte aligned");
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err; }
+
+int moe_num_sms(void) { return moe::num_sms(); }
+
+moe_status moe_get_device_status(moe_stream_t stream, int* status) {
+    REQUIRE(status, "moe_get_device_status: null status");
+    CUDA_OK(cudaStreamSynchronize(stream));
+    int v = 0, zero = 0;
+    CUDA_OK(cudaMemcpyFromSymbol(&v, moe::g_device_status, sizeof(int)));
+    CUDA_OK(cudaMemcpyToSymbol(moe::g_device_status, &zero, sizeof(int)));
+    *status = v;
+    return MOE_OK;
+}
+
+moe_status fp8_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld_x, uint8_t* q, float* scales,
+                           int64_t ld_s, moe_stream_t stream) {
+    REQUIRE(rows >= 0 && cols > 0 && cols % 128 == 0, "fp8_quant_1x128: cols=%lld must be a multiple of 128",
+            (long long)cols);
+    REQUIRE(ld_x >= cols && ld_x % 8 == 0, "fp8_quant_1x128: ld_x must be >= cols and a multiple of 8");
+    REQUIRE(ld_s >= rows, "fp8_quant_1x128: ld_s must be >= rows");
+    if (rows == 0) return MOE_OK;
+    REQUIRE(x && q && scales, "fp8_quant_1x128: null pointer");
+    REQUIRE(al16(x) && al8(q), "fp8_quant_1x128: x must be 16-byte and q 8-byte aligned");
+    CUDA_OK(moe::launch_quant_1x128(x, rows, cols, ld_x, q, scales, ld_s, stream));
+    return MOE_OK;
+}
+
+moe_status fp8_quant_128x128(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* q, float* scales,
+                             moe_stream_t stream) {
+    REQUIRE(rows >= 0 && cols > 0 && cols % 128 == 0, "fp8_quant_128x128: cols must be a multiple of 128");
+    REQUIRE((rows + 127) / 128 <= 65535 && cols / 128 <= int64_t(1) << 30, "fp8_quant_128x128: too many blocks");
+    if (rows == 0) return MOE_OK;
+    REQUIRE(w && q && scales, "fp8_quant_128x128: null pointer");
+    REQUIRE(al16(w) && al8(q), "fp8_quant_128x128: w must be 16-byte and q 8-byte aligned");
+    CUDA_OK(moe::launch_quant_128x128(w, rows, cols, q, scales, stream));
+    return MOE_OK;
+}
+
+size_t moe_route_workspace_size(int64_t T, int d, int N, int centroid_dtype) {
+    return moe::plan_route(T, d, N, centroid_dtype).total_bytes;
+}
+
+moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype, const float* bias,
+                     int N, int K, int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
+                     float* scores, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    STATUS_OK(check_route(u, T, d, centroids, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates,
+                          loads));
+    const moe::RoutePlan plan = moe::plan_route(T, d, N, centroid_dtype);
+    if (!workspace || workspace_bytes < plan.total_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_route: workspace needs %zu bytes, 256-byte aligned", plan.total_bytes);
+    CUDA_OK(moe::launch_route(u, T, d, centroids, centroid_dtype, bias, N, K, n_groups > 1 ? n_groups : 1,
+                              n_groups > 1 ? topk_groups : 1, topk_idx, gates, loads, scores, workspace, plan, stream));
+    return MOE_OK;
+}
+
+size_t moe_permute_workspace_size(int64_t T, int N) { return moe::permute_ws_bytes(T, N); }
+
+moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K, int out_dtype,
+                       int with_shared, int32_t* offsets, int32_t* perm_token, int32_t* dest_row, void* x_perm,
+                       float* x_perm_scales, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    REQUIRE(T >= 0 && T * (K + 1) <= kMaxRows, "moe_permute: T=%lld out of range", (long long)T);
+    REQUIRE(d > 0 && d % 128 == 0, "moe_permute: d=%d must be a multiple of 128", d);
+    REQUIRE(N >= 1 && N <= 1024, "moe_permute: N=%d must be in [1, 1024]", N);
+    REQUIRE(K >= 1 && K <= 16 && K <= N, "moe_permute: K=%d", K);
+    REQUIRE(out_dtype == MOE_DTYPE_BF16 || out_dtype == MOE_DTYPE_E4M3, "moe_permute: out dtype %d", out_dtype);
+    REQUIRE(offsets, "moe_permute: null offsets");
+    if (T > 0) {
+        REQUIRE(x && topk_idx && perm_token && dest_row && x_perm, "moe_permute: null pointer");
+        REQUIRE(out_dtype != MOE_DTYPE_E4M3 || x_perm_scales, "moe_permute: E4M3 output needs scales");
+        REQUIRE(al16(x) && al16(x_perm), "moe_permute: x and x_perm must be 16-byte aligned");
+    }
+    const size_t need = moe::permute_ws_bytes(T, N);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return fail(MOE_ERR_WORKSPACE, "moe_permute: workspace needs %zu bytes", need);
+    CUDA_OK(moe::launch_permute(x, T, d, topk_idx, N, K, out_dtype, with_shared ? 1 : 0, offsets, perm_token,
+                                dest_row, x_perm, x_perm_scales, workspace, stream));
+    return MOE_OK;
+}
+
+moe_status fp8_grouped_gemm(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                            const int32_t* group_offsets, int G, int64_t M_total, int Nd, int Kd, int epilogue,
+                            void* C, float* c_scales, moe_stream_t stream) {
+    REQUIRE(G >= 1 && G <= moe::gemm_max_groups(), "fp8_grouped_gemm: G=%d must be in [1, 1024]", G);
+    REQUIRE(M_total >= 0 && M_total <= kMaxRows, "fp8_grouped_gemm: M_total out of range");
+    REQUIRE(Kd > 0 && Kd % 128 == 0, "fp8_grouped_gemm: Kd=%d must be a multiple of 128", Kd);
+    REQUIRE(Nd > 0 && Nd % 256 == 0, "fp8_grouped_gemm: Nd=%d must be a multiple of 256", Nd);
+    REQUIRE(int64_t(G) * Nd <= kMaxRows, "fp8_grouped_gemm: G*Nd too large");
+    REQUIRE(epilogue == MOE_EPI_BF16 || epilogue == MOE_EPI_SWIGLU_FP8, "fp8_grouped_gemm: epilogue %d", epilogue);
+    REQUIRE(group_offsets && B && sb, "fp8_grouped_gemm: null pointer");
+    REQUIRE(al16(B), "fp8_grouped_gemm: B must be 16-byte aligned");
+    if (M_total == 0) return MOE_OK;
+    REQUIRE(A && sa && C, "fp8_grouped_gemm: null pointer");
+    REQUIRE(epilogue != MOE_EPI_SWIGLU_FP8 || c_scales, "fp8_grouped_gemm: SwiGLU output needs scales");
+    REQUIRE(al16(A) && al16(C), "fp8_grouped_gemm: A and C must be 16-byte aligned");
+    CUtensorMap ta, tb;
+    if (!moe::make_kmajor_map(&ta, A, false, uint64_t(Kd), uint64_t(M_total), uint64_t(Kd), 128) ||
+        !moe::make_kmajor_map(&tb, B, false, uint64_t(Kd), uint64_t(G) * Nd, uint64_t(Kd), 256))
+        return fail(MOE_ERR_CUDA, "fp8_grouped_gemm: tensor map encoding failed");
+    moe::GemmArgs a{};
+    a.group_offsets = group_offsets;
+    a.G = G;
+    a.M_total = M_total;
+    a.Nd = Nd;
+    a.Kd = Kd;
+    a.k_steps = Kd / 128;
+    a.a_k_steps = Kd / 128;
+    a.elems_per_step = 128;
+    a.splits = 1;
+    a.epilogue = epilogue;
+    a.sa = sa;
+    a.lda_s = M_total;
+    a.sb = sb;
+    a.C = C;
+    a.c_scales = c_scales;
+    CUDA_OK(moe::run_grouped_gemm(moe::kModeFP8, ta, tb, a, moe::num_sms(), stream));
+    return MOE_OK;
+}
+
+moe_status bf16_grouped_gemm(const uint16_t* A, const uint16_t* B, const int32_t* group_offsets, int G,
+                             int64_t M_total, int Nd, int Kd, int epilogue, void* C, moe_stream_t stream) {
+    REQUIRE(G >= 1 && G <= moe::gemm_max_groups(), "bf16_grouped_gemm: G=%d must be in [1, 1024]", G);
+    REQUIRE(M_total >= 0 && M_total <= kMaxRows, "bf16_grouped_gemm: M_total out of range");
+    REQUIRE(Kd > 0 && Kd % 64 == 0, "bf16_grouped_gemm: Kd=%d must be a multiple of 64", Kd);
+    REQUIRE(Nd > 0 && Nd % 256 == 0, "bf16_grouped_gemm: Nd=%d must be a multiple of 256", Nd);
+    REQUIRE(int64_t(G) * Nd <= kMaxRows, "bf16_grouped_gemm: G*Nd too large");
+    REQUIRE(epilogue == MOE_EPI_BF16 || epilogue == MOE_EPI_SWIGLU_BF16 || epilogue == MOE_EPI_F32,
+            "bf16_grouped_gemm: epilogue %d", epilogue);
+    REQUIRE(group_offsets && B, "bf16_grouped_gemm: null pointer");
+    REQUIRE(al16(B), "bf16_grouped_gemm: B must be 16-byte aligned");
+    if (M_total == 0) return MOE_OK;
+    REQUIRE(A && C, "bf16_grouped_gemm: null pointer");
+    REQUIRE(al16(A) && al16(C), "bf16_grouped_gemm: A and C must be 16-byte aligned");
+    CUtensorMap ta, tb;
+    if (!moe::make_kmajor_map(&ta, A, true, uint64_t(Kd), uint64_t(M_total), uint64_t(Kd) * 2, 128) ||
+        !moe::make_kmajor_map(&tb, B, true, uint64_t(Kd), uint64_t(G) * Nd, uint64_t(Kd) * 2, 256))
+        return fail(MOE_ERR_CUDA, "bf16_grouped_gemm: tensor map encoding failed");
+    moe::GemmArgs a{};
+    a.group_offsets = group_offsets;
+    a.G = G;
+    a.M_total = M_total;
+    a.Nd = Nd;
+    a.Kd = Kd;
+    a.k_steps = Kd / 64;
+    a.a_k_steps = Kd / 64;
+    a.elems_per_step = 64;
+    a.splits = 1;
+    a.epilogue = epilogue;
+    a.C = C;
+    CUDA_OK(moe::run_grouped_gemm(moe::kModeBF16, ta, tb, a, moe::num_sms(), stream));
+    return MOE_OK;
+}
+
+moe_status moe_combine(const uint16_t* u, const uint16_t* y_shared, const uint16_t* y_perm, const float* gates,
+                       const int32_t* dest_row, int64_t T, int d, int K, int64_t R, uint16_t* out,
+                       moe_stream_t stream) {
+    REQUIRE(T >= 0 && d > 0 && d % 8 == 0, "moe_combine: d=%d must be a multiple of 8", d);
+    REQUIRE(K >= 1 && K <= 16, "moe_combine: K=%d", K);
+    if (T == 0) return MOE_OK;
+    REQUIRE(u && y_perm && gates && dest_row && out, "moe_combine: null pointer");
+    REQUIRE(al16(u) && al16(y_perm) && al16(out) && (!y_shared || al16(y_shared)),
+            "moe_combine: row pointers must be 16-byte aligned");
+    CUDA_OK(moe::launch_combine(u, y_shared, y_perm, gates, dest_row, T, d, K, R, out, stream));
+    return MOE_OK;
+}
+
+moe_status moe_bias_update(float* bias, const int32_t* loads, int N, int64_t T, int K, float gamma,
+                           moe_stream_t stream) {
+    REQUIRE(N >= 1 && T >= 0 && K >= 1, "moe_bias_update: bad sizes");
+    REQUIRE(bias && loads, "moe_bias_update: null pointer");
+    CUDA_OK(moe::launch_bias_update(bias, loads, N, T, K, gamma, stream));
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// The layer
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct LayerWs {
+    size_t route, perm, offsets, perm_token, dest_row, topk, gates, x_perm, x_scales, act, act_scales, y, u_dev,
+        out_dev, total;
+};
+
+LayerWs layer_ws(const moe_layer_weights* w, int64_t T, bool host) {
+    LayerWs L{};
+    const int64_t R = T * w->K + T;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o += up256(bytes);
+        return at;
+    };
+    L.route = take(moe::plan_route(T, w->d, w->N, w->centroid_dtype).total_bytes);
+    L.perm = take(moe::permute_ws_bytes(T, w->N));
+    L.offsets = take(size_t(w->N + 2) * 4);
+    L.perm_token = take(size_t(T) * w->K * 4);
+    L.dest_row = take(size_t(T) * w->K * 4);
+    L.topk = take(size_t(T) * w->K * 4);
+    L.gates = take(size_t(T) * w->K * 4);
+    const size_t es = w->fp8 ? 1 : 2;
+    L.x_perm = take(size_t(R) * w->d * es);
+    L.x_scales = take(w->fp8 ? size_t(w->d / 128) * R * 4 : 0);
+    L.act = take(size_t(R) * w->I * es);
+    L.act_scales = take(w->fp8 ? size_t(w->I / 128) * R * 4 : 0);
+    L.y = take(size_t(R) * w->d * 2);
+    L.u_dev = take(host ? size_t(T) * w->d * 2 : 0);
+    L.out_dev = take(host ? size_t(T) * w->d * 2 : 0);
+    L.total = o;
+    return L;
+}
+
+moe_status check_layer(const moe_layer_weights* w) {
+    REQUIRE(w, "moe_layer: null weights");
+    REQUIRE(w->d > 0 && w->d % 256 == 0, "moe_layer: d=%d must be a multiple of 256", w->d);
+    REQUIRE(w->I > 0 && w->I % 128 == 0, "moe_layer: I=%d must be a multiple of 128", w->I);
+    REQUIRE(w->N + 1 <= moe::gemm_max_groups(), "moe_layer: too many experts");
+    REQUIRE(w->w13 && w->w2 && w->centroids && w->bias, "moe_layer: null weight pointer");
+    REQUIRE(!w->fp8 || (w->w13_scales && w->w2_scales), "moe_layer: FP8 weights need scales");
+    return MOE_OK;
+}
+
+}  // namespace
+
+size_t moe_layer_workspace_size(const moe_layer_weights* w, int64_t T) { return w ? layer_ws(w, T, false).total : 0; }
+size_t moe_layer_host_workspace_size(const moe_layer_weights* w, int64_t T) {
+    return w ? layer_ws(w, T, true).total : 0;
+}
+
+static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
+                                const moe_layer_outputs* outs, int update_bias, uint8_t* ws, const LayerWs& L,
+                                moe_stream_t stream) {
+    const int K = w->K, N = w->N, d = w->d, I = w->I;
+    const int64_t R = T * K + T;
+    int32_t* topk = outs && outs->topk_idx ? outs->topk_idx : reinterpret_cast<int32_t*>(ws + L.topk);
+    float* gates = outs && outs->gates ? outs->gates : reinterpret_cast<float*>(ws + L.gates);
+    int32_t* loads = outs->loads;
+    int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    int32_t* dest = reinterpret_cast<int32_t*>(ws + L.dest_row);
+    STATUS_OK(moe_route(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups, topk,
+                        gates, loads, nullptr, ws + L.route, L.perm - L.route, stream));
+    STATUS_OK(moe_permute(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
+                          reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,
+                          reinterpret_cast<float*>(ws + L.x_scales), ws + L.perm, L.offsets - L.perm, stream));
+    if (w->fp8) {
+        STATUS_OK(fp8_grouped_gemm(ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales),
+                                   reinterpret_cast<const uint8_t*>(w->w13), w->w13_scales, offsets, N + 1, R, 2 * I, d,
+                                   MOE_EPI_SWIGLU_FP8, ws + L.act, reinterpret_cast<float*>(ws + L.act_scales),
+                                   stream));
+        STATUS_OK(fp8_grouped_gemm(ws + L.act, reinterpret_cast<float*>(ws + L.act_scales),
+                                   reinterpret_cast<const uint8_t*>(w->w2), w->w2_scales, offsets, N + 1, R, d, I,
+                                   MOE_EPI_BF16, ws + L.y, nullptr, stream));
+    } else {
+        STATUS_OK(bf16_grouped_gemm(reinterpret_cast<uint16_t*>(ws + L.x_perm),
+                                    reinterpret_cast<const uint16_t*>(w->w13), offsets, N + 1, R, 2 * I, d,
+                                    MOE_EPI_SWIGLU_BF16, ws + L.act, stream));
+        STATUS_OK(bf16_grouped_gemm(reinterpret_cast<uint16_t*>(ws + L.act), reinterpret_cast<const uint16_t*>(w->w2),
+                                    offsets, N + 1, R, d, I, MOE_EPI_BF16, ws + L.y, stream));
+    }
+    const uint16_t* y = reinterpret_cast<const uint16_t*>(ws + L.y);
+    STATUS_OK(moe_combine(u, y + T * K * int64_t(d), y, gates, dest, T, d, K, R, out, stream));
+    if (update_bias) STATUS_OK(moe_bias_update(w->bias, loads, N, T, K, w->gamma, stream));
+    return MOE_OK;
+}
+
+moe_status moe_layer_forward(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
+                             const moe_layer_outputs* outs, int update_bias, void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream) {
+    STATUS_OK(check_layer(w));
+    REQUIRE(outs && outs->loads, "moe_layer_forward: outputs need a loads buffer");
+    REQUIRE(T >= 0 && u && out, "moe_layer_forward: null u/out");
+    const LayerWs L = layer_ws(w, T, false);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_layer_forward: workspace needs %zu bytes, 256-byte aligned", L.total);
+    return layer_forward(w, u, T, out, outs, update_bias, reinterpret_cast<uint8_t*>(workspace), L, stream);
+}
+
+moe_status moe_layer_forward_host(const moe_layer_weights* w, const uint16_t* u_host, int64_t T, uint16_t* out_host,
+                                  const moe_layer_outputs* outs, int update_bias, void* workspace,
+                                  size_t workspace_bytes, moe_stream_t stream) {
+    STATUS_OK(check_layer(w));
+    REQUIRE(outs && outs->loads, "moe_layer_forward_host: outputs need a loads buffer");
+    REQUIRE(T >= 0 && u_host && out_host, "moe_layer_forward_host: null u/out");
+    const LayerWs L = layer_ws(w, T, true);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_layer_forward_host: workspace needs %zu bytes", L.total);
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    uint16_t* u_dev = reinterpret_cast<uint16_t*>(ws + L.u_dev);
+    uint16_t* out_dev = reinterpret_cast<uint16_t*>(ws + L.out_dev);
+    const size_t bytes = size_t(T) * w->d * 2;
+    CUDA_OK(cudaMemcpyAsync(u_dev, u_host, bytes, cudaMemcpyHostToDevice, stream));
+    STATUS_OK(layer_forward(w, u_dev, T, out_dev, outs, update_bias, ws, L, stream));
+    CUDA_OK(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, stream));
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,473 @@
+// Grouped GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// One persistent, warp-specialised kernel serves three uses:
+//   * FP8 expert GEMMs with fine-grained scales (DeepSeek-V3 Technical Report,
+//     learn.ifs.name summary, paragraphs on FP8 tiles and on promotion): each
+//     128-wide K block is multiplied by the tensor cores into its own TMEM
+//     buffer; epilogue warps read it, multiply by sa[row,kb] * sb[nblk,kb]
+//     and add it into FP32 registers, while the tensor cores fill the other
+//     buffer with the next block.
+//   * bf16 expert GEMMs (FP32 accumulation over the whole K in TMEM).
+//   * the gate logits of routing (bf16, split-K partial sums in fp32).
+//
+// Block roles (576 threads):
+//   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and, in
+//               warpgroup w/4, the columns {32*(w/4) + c} and {128 + 32*(w/4) + c};
+//   warp 16     TMA producer (one elected lane);
+//   warp 17     tcgen05.mma issuer (one elected lane) + TMEM owner.
+// Tile: 128 rows x 256 columns, K step 128 bytes (128 e4m3 or 64 bf16),
+// 4-stage shared-memory ring (48 KB per stage), 2 x 256 TMEM columns.
+#include "common.cuh"
+#include "gemm.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBM = 128, kBN = 256;
+constexpr int kABytes = kBM * 128, kBBytes = kBN * 128;
+constexpr int kEpiWarps = 16, kThreads = (kEpiWarps + 2) * 32;
+constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+constexpr int kMaxGroups = 1024;
+
+struct Smem {
+    uint64_t full[kStages], empty[kStages];
+    uint64_t tfull[2], tempty[2], xchg[2], drain;
+    uint32_t tmem_base;
+    int abort;
+    int total_items;
+    float amax[2][4][128];
+    int prefix[kMaxGroups + 1];
+    int offs[kMaxGroups + 1];
+};
+constexpr size_t kRingBytes = size_t(kStages) * (kABytes + kBBytes);
+constexpr size_t kSmemBytes = kRingBytes + sizeof(Smem) + 1024;
+
+struct Item {
+    int g, mt, nt, sp;
+};
+
+__device__ __forceinline__ Item decode(int item, const Smem& s, int G, int n_tiles_n, int splits) {
+    int lo = 0, hi = G;  // prefix[lo] <= item < prefix[hi]
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (s.prefix[mid] <= item) lo = mid;
+        else hi = mid;
+    }
+    Item it;
+    it.g = lo;
+    int local = item - s.prefix[lo];
+    it.sp = local % splits;
+    local /= splits;
+    int m_tiles = (s.offs[lo + 1] - s.offs[lo] + kBM - 1) / kBM;
+    it.mt = local % m_tiles;
+    it.nt = local / m_tiles;
+    return it;
+}
+
+__device__ __forceinline__ float silu(float x) { return __fdiv_rn(x, 1.0f + expf(-x)); }
+
+template <int kMode, int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem& s = *reinterpret_cast<Smem*>(ring + kRingBytes);
+    const uint32_t ringA = smem_u32(ring);
+    const uint32_t ringB = ringA + kStages * kABytes;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = args.G;
+    const int n_tiles_n = args.Nd / kBN;
+    const int splits = args.splits;
+    const int steps_per_split = (args.k_steps + splits - 1) / splits;
+    volatile int* abort = &s.abort;
+
+    // ---------------- prologue ----------------
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&s.full[i]), 1);
+            mbar_init(smem_u32(&s.empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s.tfull[i]), 1);
+            mbar_init(smem_u32(&s.tempty[i]), kEpiWarps);
+            mbar_init(smem_u32(&s.xchg[i]), kEpiWarps * 32);
+        }
+        mbar_init(smem_u32(&s.drain), 1);
+        s.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&s.tmem_base), 512);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 0) {
+        // group row offsets and the running count of work items per group
+        int running = 0;
+        bool bad = false;
+        for (int base = 0; base <= G; base += 32) {
+            int g = base + lane;
+            int off = 0;
+            if (g <= G) {
+                off = args.group_offsets ? args.group_offsets[g] : (g == 0 ? 0 : (int)args.M_total);
+                s.offs[g] = off;
+            }
+            __syncwarp();
+            int items = 0;
+            if (g < G) {
+                int nxt = args.group_offsets ? args.group_offsets[g + 1] : (int)args.M_total;
+                int rows = nxt - off;
+                if (rows < 0 || off < 0 || nxt > args.M_total) bad = true;
+                items = rows > 0 ? ((rows + kBM - 1) / kBM) * n_tiles_n * splits : 0;
+            }
+            int incl = items;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (g <= G) s.prefix[g] = running + incl - items;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (args.group_offsets && args.group_offsets[0] != 0) bad = true;
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            s.total_items = bad ? 0 : running;
+            if (bad && blockIdx.x == 0) report(MOE_ERR_DEVICE_DATA);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    const int total = s.total_items;
+
+    if (warp == kProducerWarp) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int armed[kStages] = {0, 0, 0, 0};
+            for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+                Item it = decode(item, s, G, n_tiles_n, splits);
+                const int a_row = s.offs[it.g] + it.mt * kBM;
+                const int b_row = it.g * args.Nd + it.nt * kBN;
+                const int k0 = it.sp * steps_per_split;
+                const int k1 = min(args.k_steps, k0 + steps_per_split);
+                bool ok = true;
+                for (int ks = k0; ks < k1; ++ks) {
+                    if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&s.full[stage]);
+                    mbar_arrive_expect_tx(fb, kABytes + kBBytes);
+                    tma_load_2d(ringA + stage * kABytes, &tmA, fb, (ks % args.a_k_steps) * args.elems_per_step,
+                                a_row);
+                    tma_load_2d(ringB + stage * kBBytes, &tmB, fb, ks * args.elems_per_step, b_row);
+                    armed[stage] += 1;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            // never leave the block while a copy into its shared memory is in flight
+            for (int i = 0; i < kStages; ++i)
+                if (armed[i] > 0) mbar_wait_limit(smem_u32(&s.full[i]), uint32_t(armed[i] - 1) & 1u, 200000000ull);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ---------------- tcgen05.mma issuer ----------------
+        constexpr uint32_t idesc = kMode == kModeFP8 ? make_idesc(0, 0, kBM, kBN) : make_idesc(1, 1, kBM, kBN);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t acc_iter = 0;
+        for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+            Item it = decode(item, s, G, n_tiles_n, splits);
+            const int k0 = it.sp * steps_per_split;
+            const int k1 = min(args.k_steps, k0 + steps_per_split);
+            uint32_t buf = acc_iter & 1u;
+            bool ok = true;
+            if (kMode != kModeFP8) {
+                if (!mbar_wait(smem_u32(&s.tempty[buf]), ((acc_iter >> 1) & 1u) ^ 1u, abort)) break;
+                tc_fence_after();
+            }
+            for (int ks = k0; ks < k1; ++ks) {
+                if (kMode == kModeFP8) {
+                    buf = acc_iter & 1u;
+                    if (!mbar_wait(smem_u32(&s.tempty[buf]), ((acc_iter >> 1) & 1u) ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!mbar_wait(smem_u32(&s.full[stage]), phase, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t ad = smem_desc_sw128(ringA + stage * kABytes);
+                    const uint64_t bd = smem_desc_sw128(ringB + stage * kBBytes);
+                    const uint32_t d = tmem_base + buf * kBN;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t acc = (k > 0 || (kMode != kModeFP8 && ks > k0)) ? 1u : 0u;
+                        if (kMode == kModeFP8) mma_e4m3(d, ad + 2 * k, bd + 2 * k, idesc, acc);
+                        else mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, acc);
+                    }
+                    tc_commit(smem_u32(&s.empty[stage]));
+                    if (kMode == kModeFP8) tc_commit(smem_u32(&s.tfull[buf]));
+                }
+                __syncwarp();
+                if (kMode == kModeFP8) acc_iter += 1;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (kMode != kModeFP8) {
+                if (lane == 0) tc_commit(smem_u32(&s.tfull[buf]));
+                __syncwarp();
+                acc_iter += 1;
+            }
+        }
+        // every issued MMA must be complete before TMEM is freed
+        if (lane == 0) {
+            tc_commit(smem_u32(&s.drain));
+            mbar_wait_limit(smem_u32(&s.drain), 0, 200000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue warps ----------------
+        const int q = warp & 3;        // TMEM lane quarter = rows 32q..32q+31
+        const int wg = warp >> 2;      // column slice
+        const int row_in_tile = q * 32 + lane;
+        const uint32_t lane_addr = tmem_base + (uint32_t(q * 32) << 16);
+        uint32_t acc_iter = 0, tile_iter = 0;
+        for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+            Item it = decode(item, s, G, n_tiles_n, splits);
+            const int k0 = it.sp * steps_per_split;
+            const int k1 = min(args.k_steps, k0 + steps_per_split);
+            const int rows_g = s.offs[it.g + 1] - s.offs[it.g];
+            const int row_local = it.mt * kBM + row_in_tile;
+            const bool valid = row_local < rows_g;
+            const int64_t grow = int64_t(s.offs[it.g]) + row_local;
+            float acc[64];
+            bool ok = true;
+            if (kMode == kModeFP8) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
+                const int nkb = args.Kd / 128;
+                const float* sb_lo = args.sb + (int64_t(it.g) * (args.Nd / 128) + 2 * it.nt) * nkb;
+                // rows past the group's end read row 0's scale (never stored)
+                const float* sa_p = args.sa + (valid ? grow : 0) + int64_t(k0) * args.lda_s;
+                const uint32_t lda = uint32_t(args.lda_s);
+                float sa0 = __ldg(sa_p);
+                float fl_n = sa0 * __ldg(sb_lo + k0), fh_n = sa0 * __ldg(sb_lo + nkb + k0);
+                for (int ks = k0; ks < k1; ++ks) {
+                    const float fl = fl_n, fh = fh_n;
+                    if (ks + 1 < k1) {
+                        sa_p += lda;
+                        const float sa1 = __ldg(sa_p);
+                        fl_n = sa1 * __ldg(sb_lo + ks + 1);
+                        fh_n = sa1 * __ldg(sb_lo + nkb + ks + 1);
+                    }
+                    const uint32_t buf = acc_iter & 1u;
+                    if (!mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t col = lane_addr + buf * kBN + wg * 32;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        // chunks 0,1: columns 32*wg + 0..31 (first weight block);
+                        // chunks 2,3: 128 + 32*wg + 0..31 (second weight block)
+                        uint32_t r[16];
+                        tmem_ld_16(col + (c >> 1) * 128 + (c & 1) * 16, r);
+                        tmem_wait_ld(r);
+                        if (c == 3) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+                        }
+                        const float f = c < 2 ? fl : fh;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(__uint_as_float(r[i]), f, acc[c * 16 + i]);
+                    }
+                    acc_iter += 1;
+                }
+            } else {
+                const uint32_t buf = tile_iter & 1u;
+                if (!mbar_wait(smem_u32(&s.tfull[buf]), (tile_iter >> 1) & 1u, abort)) break;
+                tc_fence_after();
+                const uint32_t col = lane_addr + buf * kBN + wg * 32;
+                uint32_t r0[32], r1[32];
+                tmem_ld_32(col, r0);
+                tmem_ld_32(col + 128, r1);
+                tmem_wait_ld(r0, r1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    acc[i] = __uint_as_float(r0[i]);
+                    acc[32 + i] = __uint_as_float(r1[i]);
+                }
+            }
+            if (!ok) break;
+
+            // ---- epilogue of the tile ----
+            constexpr int ep = kEpi;
+            if constexpr (ep == MOE_EPI_SWIGLU_FP8 || ep == MOE_EPI_SWIGLU_BF16) {
+                float a[32];
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    a[i] = silu(acc[i]) * acc[32 + i];
+                    amax = fmaxf(amax, fabsf(a[i]));
+                }
+                const int64_t ocol = int64_t(it.nt) * 128 + wg * 32;
+                const int64_t ldo = args.Nd / 2;
+                if constexpr (ep == MOE_EPI_SWIGLU_FP8) {
+                    const uint32_t par = tile_iter & 1u;
+                    s.amax[par][wg][row_in_tile] = amax;
+                    mbar_arrive(smem_u32(&s.xchg[par]));
+                    if (!mbar_wait(smem_u32(&s.xchg[par]), (tile_iter >> 1) & 1u, abort)) break;
+                    amax = fmaxf(fmaxf(s.amax[par][0][row_in_tile], s.amax[par][1][row_in_tile]),
+                                 fmaxf(s.amax[par][2][row_in_tile], s.amax[par][3][row_in_tile]));
+                    const float sc = tile_scale(amax);
+                    if (valid) {
+                        uint8_t* out = reinterpret_cast<uint8_t*>(args.C) + grow * ldo + ocol;
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t p0 = pack_e4m3x2(__fdiv_rn(a[4 * i], sc), __fdiv_rn(a[4 * i + 1], sc));
+                            const uint32_t p1 =
+                                pack_e4m3x2(__fdiv_rn(a[4 * i + 2], sc), __fdiv_rn(a[4 * i + 3], sc));
+                            w[i] = p0 | (p1 << 16);
+                        }
+                        reinterpret_cast<uint4*>(out)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4*>(out)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        if (wg == 0) args.c_scales[int64_t(it.nt) * args.M_total + grow] = sc;
+                    }
+                } else if (valid) {
+                    uint16_t* out = reinterpret_cast<uint16_t*>(args.C) + grow * ldo + ocol;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 pk = make_uint4(pack_bf16x2(a[8 * v], a[8 * v + 1]), pack_bf16x2(a[8 * v + 2], a[8 * v + 3]),
+                                              pack_bf16x2(a[8 * v + 4], a[8 * v + 5]),
+                                              pack_bf16x2(a[8 * v + 6], a[8 * v + 7]));
+                        reinterpret_cast<uint4*>(out)[v] = pk;
+                    }
+                }
+            } else if (valid) {
+                const int64_t c0 = int64_t(it.nt) * kBN + wg * 32;
+                if constexpr (ep == MOE_EPI_BF16) {
+                    uint16_t* out = reinterpret_cast<uint16_t*>(args.C) + grow * args.Nd + c0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float* x = acc + 32 * h + 8 * v;
+                            uint4 pk = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                                  pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+                            reinterpret_cast<uint4*>(out + 128 * h)[v] = pk;
+                        }
+                } else {  // MOE_EPI_F32: split-K partial sums, [splits][M_total][Nd]
+                    float* out = reinterpret_cast<float*>(args.C) + (int64_t(it.sp) * args.M_total + grow) * args.Nd + c0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            const float* x = acc + 32 * h + 4 * v;
+                            reinterpret_cast<float4*>(out + 128 * h)[v] = make_float4(x[0], x[1], x[2], x[3]);
+                        }
+                }
+            }
+            tile_iter += 1;
+        }
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+// 2-D K-major tensor map: `rows` rows of `inner` elements (row stride
+// `row_bytes`), box = 128 bytes of K x `box_rows` rows, 128-byte swizzle,
+// out-of-range rows read as zero.
+bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                     uint32_t box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {bf16 ? 64u : 128u, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int kMode, int kEpi>
+static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
+                          cudaStream_t stream) {
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kMode, kEpi>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    grouped_gemm_kernel<kMode, kEpi><<<grid, kThreads, kSmemBytes, stream>>>(a, b, args);
+    return cudaGetLastError();
+}
+
+cudaError_t run_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
+                             cudaStream_t stream) {
+    if (mode == kModeFP8) {
+        if (args.epilogue == MOE_EPI_SWIGLU_FP8) return launch<kModeFP8, MOE_EPI_SWIGLU_FP8>(a, b, args, grid, stream);
+        if (args.epilogue == MOE_EPI_BF16) return launch<kModeFP8, MOE_EPI_BF16>(a, b, args, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (args.epilogue == MOE_EPI_SWIGLU_BF16) return launch<kModeBF16, MOE_EPI_SWIGLU_BF16>(a, b, args, grid, stream);
+    if (args.epilogue == MOE_EPI_BF16) return launch<kModeBF16, MOE_EPI_BF16>(a, b, args, grid, stream);
+    if (args.epilogue == MOE_EPI_F32) return launch<kModeBF16, MOE_EPI_F32>(a, b, args, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+int gemm_max_groups() { return kMaxGroups; }
+
+}  // namespace moe

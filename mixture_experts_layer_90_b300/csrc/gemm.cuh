@@ -1,0 +1,38 @@
+// Host-side interface of the tcgen05 grouped GEMM kernel (gemm.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+enum { kModeFP8 = 0, kModeBF16 = 1 };
+
+struct GemmArgs {
+    const int32_t* group_offsets;  // [G+1] device; nullptr = one group of M_total rows
+    int G;
+    int64_t M_total;
+    int Nd;              // output columns per group, multiple of 256
+    int Kd;              // K extent of B in elements (FP8: also of A)
+    int k_steps;         // 128-byte K steps per output tile (before split)
+    int a_k_steps;       // A's K extent in steps; A's step = step % a_k_steps
+    int elems_per_step;  // 128 (e4m3) or 64 (bf16)
+    int splits;          // split-K parts (MOE_EPI_F32 only; else 1)
+    int epilogue;        // MOE_EPI_*
+    const float* sa;     // FP8: [Kd/128][lda_s] activation scales
+    int64_t lda_s;
+    const float* sb;     // FP8: [G][Nd/128][Kd/128] weight scales
+    void* C;
+    float* c_scales;     // MOE_EPI_SWIGLU_FP8: [Nd/256][M_total]
+};
+
+bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inner, uint64_t rows,
+                     uint64_t row_bytes, uint32_t box_rows);
+
+cudaError_t run_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
+                             cudaStream_t stream);
+
+int gemm_max_groups();
+
+}  // namespace moe

@@ -1,0 +1,112 @@
+"""MoELayer: device-resident weights of one DeepSeekMoE layer and its forward.
+
+The layer formula (nlp-lineage.vercel.app "DeepSeek-V3 Technical Report
+(2024)", "The notation"): h'_t = u_t + FFN_shared(u_t) + sum_i g_{i,t} FFN_i(u_t),
+one shared expert and N routed experts (top-K), every FFN a SwiGLU MLP whose
+weights live in HBM as E4M3 with 128x128 block scales (or bf16).
+
+Layout (all device memory, allocated once here, never by the C library):
+  w13 [N+1, 2I, d]  gate and up projections, rows interleaved per 128
+                    (gate rows 128j.., then up rows 128j..), expert N = shared
+  w2  [N+1, d, I]   down projections
+  *_scales          fp32 [N+1, rows/128, cols/128]
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import (MOE_DTYPE_BF16, MOE_DTYPE_F32, LayerOutputs, LayerWeights, _check, _p, _require_cuda, _stream,
+               fp8_quant_128x128, load_library)
+
+
+def interleave_gate_up(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
+    """[I, d] gate and [I, d] up -> [2I, d] with 128-row blocks alternating."""
+    I, d = w1.shape
+    return torch.stack((w1.view(I // 128, 128, d), w3.view(I // 128, 128, d)), dim=1).reshape(2 * I, d)
+
+
+class MoELayer:
+    def __init__(self, d, N, K, I, centroids, bias, w13, w2, w13_scales=None, w2_scales=None, n_groups=1,
+                 topk_groups=1, gamma=1e-3):
+        _require_cuda()
+        self.d, self.N, self.K, self.I = d, N, K, I
+        self.n_groups, self.topk_groups, self.gamma = n_groups, topk_groups, gamma
+        self.fp8 = w13.dtype == torch.uint8
+        self.centroids, self.bias = centroids, bias
+        self.w13, self.w2, self.w13_scales, self.w2_scales = w13, w2, w13_scales, w2_scales
+        self._desc = LayerWeights(
+            d=d, N=N, K=K, I=I, n_groups=n_groups, topk_groups=topk_groups, gamma=gamma, fp8=int(self.fp8),
+            centroids=centroids.data_ptr(),
+            centroid_dtype=MOE_DTYPE_F32 if centroids.dtype == torch.float32 else MOE_DTYPE_BF16,
+            bias=bias.data_ptr(), w13=w13.data_ptr(),
+            w13_scales=w13_scales.data_ptr() if w13_scales is not None else None,
+            w2=w2.data_ptr(), w2_scales=w2_scales.data_ptr() if w2_scales is not None else None)
+        self._ws = {}
+        self.loads = torch.zeros((N,), dtype=torch.int32, device=centroids.device)
+
+    @classmethod
+    def build(cls, d, N, K, I, centroids, bias, expert_weights, fp8=True, **kw):
+        """expert_weights(e) -> (w1 [I,d], w3 [I,d], w2 [d,I]) bf16 device tensors for
+        e in 0..N (N = shared expert); quantised here per 128x128 block when fp8."""
+        dev = centroids.device
+        G = N + 1
+        if fp8:
+            w13 = torch.empty((G, 2 * I, d), dtype=torch.uint8, device=dev)
+            w2 = torch.empty((G, d, I), dtype=torch.uint8, device=dev)
+            s13 = torch.empty((G, 2 * I // 128, d // 128), dtype=torch.float32, device=dev)
+            s2 = torch.empty((G, d // 128, I // 128), dtype=torch.float32, device=dev)
+        else:
+            w13 = torch.empty((G, 2 * I, d), dtype=torch.bfloat16, device=dev)
+            w2 = torch.empty((G, d, I), dtype=torch.bfloat16, device=dev)
+            s13 = s2 = None
+        for e in range(G):
+            w1, w3, w2e = expert_weights(e)
+            w13e = interleave_gate_up(w1, w3)
+            if fp8:
+                fp8_quant_128x128(w13e, w13[e], s13[e])
+                fp8_quant_128x128(w2e.contiguous(), w2[e], s2[e])
+            else:
+                w13[e].copy_(w13e)
+                w2[e].copy_(w2e)
+        return cls(d, N, K, I, centroids, bias, w13, w2, s13, s2, **kw)
+
+    def workspace(self, T: int, host: bool = False) -> torch.Tensor:
+        key = (T, host)
+        ws = self._ws.get(key)
+        if ws is None:
+            L = load_library()
+            f = L.moe_layer_host_workspace_size if host else L.moe_layer_workspace_size
+            need = f(ctypes.byref(self._desc), T)
+            ws = torch.empty((max(int(need), 1),), dtype=torch.uint8, device=self.centroids.device)
+            self._ws[key] = ws
+        return ws
+
+    def _outs(self, topk_idx, gates):
+        return LayerOutputs(topk_idx=topk_idx.data_ptr() if topk_idx is not None else None,
+                            gates=gates.data_ptr() if gates is not None else None,
+                            loads=self.loads.data_ptr())
+
+    def forward(self, u: torch.Tensor, out: torch.Tensor = None, update_bias: bool = True, topk_idx=None,
+                gates=None) -> torch.Tensor:
+        """u bf16 [T, d] on the device -> h' bf16 [T, d]; then the bias update."""
+        T = u.shape[0]
+        out = torch.empty_like(u) if out is None else out
+        ws = self.workspace(T)
+        outs = self._outs(topk_idx, gates)
+        _check(load_library().moe_layer_forward(ctypes.byref(self._desc), _p(u), T, _p(out), ctypes.byref(outs),
+                                                int(update_bias), _p(ws), ws.numel(), _stream()),
+               "moe_layer_forward")
+        return out
+
+    def forward_host(self, u_host: torch.Tensor, out_host: torch.Tensor, update_bias: bool = True):
+        """Same with u/h' in (pinned) host memory: copies in and out inside the call."""
+        T = u_host.shape[0]
+        ws = self.workspace(T, host=True)
+        outs = self._outs(None, None)
+        _check(load_library().moe_layer_forward_host(ctypes.byref(self._desc), ctypes.c_void_p(u_host.data_ptr()), T,
+                                                     ctypes.c_void_p(out_host.data_ptr()), ctypes.byref(outs),
+                                                     int(update_bias), _p(ws), ws.numel(), _stream()),
+               "moe_layer_forward_host")
+        return out_host

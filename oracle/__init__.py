@@ -314,3 +314,54 @@ def expert_ffn_bf16(x_bf16, w1, w3, w2):
     h3 = bf16_gemm(x_bf16, w3)
     a = bf16_round(swiglu(h1, h3))
     return bf16_gemm(a, w2)
+
+
+def layer_tokens(u_bf16, centroids, bias, K, expert_weights, tokens, fp8=True, n_groups=1, topk_groups=1,
+                 delta=0.0, route_all=None):
+    """h' in FP64 for the listed tokens (nlp-lineage page, "The notation"):
+
+        h'_t = u_t + FFN_shared(u_t) + sum_k g_{t,k} FFN_{idx[t,k]}(u_t)
+
+    expert_weights(e) -> (w1, w3, w2) bf16 (e = N is the shared expert).
+    Routing is the oracle's own (route_all, a Route of all tokens, may be
+    passed in to avoid recomputing it). The FP8 path quantises each token row
+    per 1x128 tile, every weight per 128x128 block and the intermediate per
+    1x128 tile; the bf16 path rounds the intermediate and y to bf16 where the
+    bf16 kernels store them. Returns (h' [n, d], route of all tokens, and per
+    token the expert outputs' boundary-distance details for the FP8 path).
+    """
+    import torch
+    tokens = np.asarray(tokens, dtype=np.int64)
+    r = route_all if route_all is not None else route(u_bf16, centroids, bias, K, n_groups, topk_groups, delta)
+    u_bits = as_bf16_bits(u_bf16)[tokens]
+    T_s, d = u_bits.shape
+    N = (centroids.shape[0])
+    idx = r.topk_idx[tokens]
+    g = r.gates[tokens]
+    if fp8:
+        xq, xs = quant_1x128(u_bits)
+    y_tok = np.zeros((T_s, K, d))
+    y_sh = None
+    detail = {}
+    for e in range(N + 1):
+        if e == N:
+            rows = np.arange(T_s)
+            ks = None
+        else:
+            rows, ks = np.nonzero(idx == e)
+        if rows.size == 0:
+            continue
+        w1, w3, w2 = expert_weights(e)
+        if fp8:
+            y, det = expert_ffn_fp8(xq[rows], xs[rows], w1, w3, w2, want_detail=True)
+            detail[e] = (rows, det)
+        else:
+            y = bf16_value(bf16_round(expert_ffn_bf16(u_bits[rows], w1, w3, w2)))
+        if fp8:
+            y = bf16_value(bf16_round(y))       # the CUDA path stores expert outputs as bf16
+        if e == N:
+            y_sh = y
+        else:
+            y_tok[rows, ks] = y
+    h = bf16_value(u_bits) + y_sh + np.einsum("tk,tkd->td", g, y_tok)
+    return h, r, detail

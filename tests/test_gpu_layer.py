@@ -1,0 +1,117 @@
+"""The whole layer on the GPU (route, permute, grouped SwiGLU GEMMs with the
+shared expert, combine, bias update) against the oracle's FP64 chain.
+
+Layer formula: nlp-lineage.vercel.app "DeepSeek-V3 Technical Report (2024)",
+"The notation". h' must be within the bf16-rounding rule of tests/helpers.py
+at tau = 2e-3 (normwise per token); routing, loads and the bias bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as S
+from helpers import check_bf16
+
+pytestmark = pytest.mark.gpu
+
+DELTA = 2e-6
+
+
+def _lib():
+    import mixture_experts_layer_90_b300 as m
+    return m
+
+
+def _build(sh, zipf=False, zero_bias=False):
+    m = _lib()
+    cent = S.centroids(sh, zipf=zipf).cuda()
+    bias = S.bias(sh, zero=zero_bias).cuda()
+    layer = m.MoELayer.build(sh.d, sh.N, sh.K, sh.I, cent, bias,
+                             lambda e: S.expert_weights(sh, e, device="cuda"), fp8=sh.fp8,
+                             n_groups=sh.n_groups, topk_groups=sh.topk_groups, gamma=sh.gamma)
+    return layer
+
+
+def _cpu_weights(sh):
+    return lambda e: tuple(w.cpu() for w in S.expert_weights(sh, e, device="cuda"))
+
+
+def _run_and_check(sh, tokens=None, zipf=False, zero_bias=False, u_seed=0):
+    m = _lib()
+    layer = _build(sh, zipf=zipf, zero_bias=zero_bias)
+    b0 = layer.bias.cpu().numpy().copy()
+    u = S.tokens(sh, seed=u_seed)
+    T = sh.T
+    idx = torch.empty((T, sh.K), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, sh.K), dtype=torch.float32, device="cuda")
+    out = layer.forward(u.cuda(), topk_idx=idx, gates=gates, update_bias=True)
+    assert m.device_status() == 0
+    idx_g, loads_g = idx.cpu().numpy(), layer.loads.cpu().numpy()
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens)
+    ref, r, _ = oracle.layer_tokens(u, layer.centroids.cpu(), torch.from_numpy(b0), sh.K, _cpu_weights(sh), tokens,
+                                    fp8=sh.fp8, n_groups=sh.n_groups, topk_groups=sh.topk_groups, delta=DELTA)
+    same = np.all(idx_g == r.topk_idx, axis=1)
+    assert np.all(same | r.near_tie), "token with a certified gap routed differently"
+    np.testing.assert_array_equal(loads_g, np.bincount(idx_g.ravel(), minlength=sh.N))
+    if same.all():
+        np.testing.assert_array_equal(loads_g, r.loads)
+    # bias after the step: one fp32 step from this step's loads
+    np.testing.assert_array_equal(layer.bias.cpu().numpy(), oracle.bias_update(b0, loads_g, T, sh.K, sh.gamma))
+    keep = same[tokens]
+    got = out[torch.as_tensor(tokens[keep]).cuda()].cpu()
+    tau = check_bf16(got, ref[keep], tau=2e-3, what=sh.name)
+    return tau, int((~same).sum())
+
+
+def test_layer_tiny_bf16():
+    """The tiny bf16 layer: T=128, d=256, 16 routed + 1 shared, top-4, I=128, b=0."""
+    tau, _ = _run_and_check(S.TINY, zero_bias=True)
+    assert tau < 2e-3
+
+
+def test_layer_small_fp8_ragged():
+    sh = S.LayerShape(T=301, d=512, N=32, K=4, I=256, name="small-fp8")
+    _run_and_check(sh)
+
+
+def test_layer_small_fp8_group_limited():
+    sh = S.LayerShape(T=96, d=512, N=64, K=6, I=256, n_groups=8, topk_groups=3, name="small-fp8-groups")
+    _run_and_check(sh)
+
+
+def test_layer_second_step_uses_updated_bias():
+    sh = S.LayerShape(T=128, d=256, N=16, K=4, I=128, name="two-steps")
+    layer = _build(sh)
+    u = S.tokens(sh).cuda()
+    layer.forward(u)
+    b1 = layer.bias.clone()
+    l1 = layer.loads.clone()
+    layer.forward(u)
+    b_exp = oracle.bias_update(b1.cpu().numpy(), layer.loads.cpu().numpy(), sh.T, sh.K, sh.gamma)
+    np.testing.assert_array_equal(layer.bias.cpu().numpy(), b_exp)
+    assert not torch.equal(b1, S.bias(sh).cuda()) or l1.sum() == sh.T * sh.K
+
+
+def test_layer_empty_batch():
+    sh = S.LayerShape(T=0, d=256, N=16, K=4, I=128, name="empty")
+    layer = _build(sh)
+    b0 = layer.bias.clone()
+    out = layer.forward(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"))
+    assert out.shape == (0, 256) and _lib().device_status() == 0
+    # no tokens: every expert is underloaded only if the mean (0) exceeds its load, which never happens
+    assert torch.equal(layer.bias, b0)
+
+
+def test_layer_host_buffers_match_device_path():
+    sh = S.LayerShape(T=200, d=512, N=32, K=4, I=256, name="host")
+    layer = _build(sh)
+    u = S.tokens(sh)
+    out_d = layer.forward(u.cuda(), update_bias=False).cpu()
+    u_h = u.pin_memory()
+    out_h = torch.empty_like(u_h).pin_memory()
+    layer.forward_host(u_h, out_h, update_bias=False)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16), out_d.view(torch.int16))
