@@ -208,7 +208,13 @@ typedef struct {
     int32_t* topk_idx;         /* [T, K] */
     float* gates;              /* [T, K] */
     int32_t* loads;            /* [N], required */
+    /* NULL, or MOE_LAYER_STAGES + 1 cudaEvent_t recorded on `stream` before the
+     * first stage and after each stage (route, permute, GEMM 1, GEMM 2,
+     * combine, bias update) — for timing the stages inside a run. */
+    void* const* stage_events;
 } moe_layer_outputs;
+
+#define MOE_LAYER_STAGES 6
 
 size_t moe_layer_workspace_size(const moe_layer_weights* w, int64_t T);
 

@@ -52,7 +52,11 @@ class LayerWeights(ctypes.Structure):
 
 class LayerOutputs(ctypes.Structure):
     """Mirror of moe_layer_outputs."""
-    _fields_ = [("topk_idx", ctypes.c_void_p), ("gates", ctypes.c_void_p), ("loads", ctypes.c_void_p)]
+    _fields_ = [("topk_idx", ctypes.c_void_p), ("gates", ctypes.c_void_p), ("loads", ctypes.c_void_p),
+                ("stage_events", ctypes.c_void_p)]
+
+
+LAYER_STAGES = ("route", "permute", "gemm1_swiglu", "gemm2", "combine", "bias_update")
 
 
 _lib = None

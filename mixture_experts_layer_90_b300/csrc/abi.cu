@@ -322,16 +322,25 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
     int32_t* loads = outs->loads;
     int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
     int32_t* dest = reinterpret_cast<int32_t*>(ws + L.dest_row);
+    void* const* ev = outs ? outs->stage_events : nullptr;
+    auto mark = [&](int i) -> moe_status {
+        if (ev) CUDA_OK(cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), stream));
+        return MOE_OK;
+    };
+    STATUS_OK(mark(0));
     STATUS_OK(moe_route(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups, topk,
                         gates, loads, nullptr, ws + L.route, L.perm - L.route, stream));
+    STATUS_OK(mark(1));
     STATUS_OK(moe_permute(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
                           reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,
                           reinterpret_cast<float*>(ws + L.x_scales), ws + L.perm, L.offsets - L.perm, stream));
+    STATUS_OK(mark(2));
     if (w->fp8) {
         STATUS_OK(fp8_grouped_gemm(ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales),
                                    reinterpret_cast<const uint8_t*>(w->w13), w->w13_scales, offsets, N + 1, R, 2 * I, d,
                                    MOE_EPI_SWIGLU_FP8, ws + L.act, reinterpret_cast<float*>(ws + L.act_scales),
                                    stream));
+        STATUS_OK(mark(3));
         STATUS_OK(fp8_grouped_gemm(ws + L.act, reinterpret_cast<float*>(ws + L.act_scales),
                                    reinterpret_cast<const uint8_t*>(w->w2), w->w2_scales, offsets, N + 1, R, d, I,
                                    MOE_EPI_BF16, ws + L.y, nullptr, stream));
@@ -339,12 +348,16 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
         STATUS_OK(bf16_grouped_gemm(reinterpret_cast<uint16_t*>(ws + L.x_perm),
                                     reinterpret_cast<const uint16_t*>(w->w13), offsets, N + 1, R, 2 * I, d,
                                     MOE_EPI_SWIGLU_BF16, ws + L.act, stream));
+        STATUS_OK(mark(3));
         STATUS_OK(bf16_grouped_gemm(reinterpret_cast<uint16_t*>(ws + L.act), reinterpret_cast<const uint16_t*>(w->w2),
                                     offsets, N + 1, R, d, I, MOE_EPI_BF16, ws + L.y, stream));
     }
+    STATUS_OK(mark(4));
     const uint16_t* y = reinterpret_cast<const uint16_t*>(ws + L.y);
     STATUS_OK(moe_combine(u, y + T * K * int64_t(d), y, gates, dest, T, d, K, R, out, stream));
+    STATUS_OK(mark(5));
     if (update_bias) STATUS_OK(moe_bias_update(w->bias, loads, N, T, K, w->gamma, stream));
+    STATUS_OK(mark(6));
     return MOE_OK;
 }
 

@@ -83,18 +83,24 @@ class MoELayer:
             self._ws[key] = ws
         return ws
 
-    def _outs(self, topk_idx, gates):
+    def _outs(self, topk_idx, gates, events=None):
+        self._ev_arr = None
+        if events is not None:
+            self._ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         return LayerOutputs(topk_idx=topk_idx.data_ptr() if topk_idx is not None else None,
                             gates=gates.data_ptr() if gates is not None else None,
-                            loads=self.loads.data_ptr())
+                            loads=self.loads.data_ptr(),
+                            stage_events=ctypes.cast(self._ev_arr, ctypes.c_void_p) if events is not None else None)
 
     def forward(self, u: torch.Tensor, out: torch.Tensor = None, update_bias: bool = True, topk_idx=None,
-                gates=None) -> torch.Tensor:
-        """u bf16 [T, d] on the device -> h' bf16 [T, d]; then the bias update."""
+                gates=None, stage_events=None) -> torch.Tensor:
+        """u bf16 [T, d] on the device -> h' bf16 [T, d]; then the bias update.
+        stage_events: optional 7 torch.cuda.Event(enable_timing=True) recorded
+        around the six stages on the current stream."""
         T = u.shape[0]
         out = torch.empty_like(u) if out is None else out
         ws = self.workspace(T)
-        outs = self._outs(topk_idx, gates)
+        outs = self._outs(topk_idx, gates, stage_events)
         _check(load_library().moe_layer_forward(ctypes.byref(self._desc), _p(u), T, _p(out), ctypes.byref(outs),
                                                 int(update_bias), _p(ws), ws.numel(), _stream()),
                "moe_layer_forward")

@@ -17,7 +17,7 @@ from helpers import check_bf16
 
 pytestmark = pytest.mark.gpu
 
-DELTA = 2e-6
+from helpers import ROUTE_DELTA as DELTA
 
 
 def _lib():
