@@ -317,6 +317,14 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
                                 moe_stream_t stream) {
     const int K = w->K, N = w->N, d = w->d, I = w->I;
     const int64_t R = T * K + T;
+    if (T == 0) {
+        // no tokens: every load is 0, equal to the mean, so the bias stays as it is
+        CUDA_OK(cudaMemsetAsync(outs->loads, 0, sizeof(int32_t) * N, stream));
+        if (outs->stage_events)
+            for (int i = 0; i <= MOE_LAYER_STAGES; ++i)
+                CUDA_OK(cudaEventRecord(reinterpret_cast<cudaEvent_t>(outs->stage_events[i]), stream));
+        return MOE_OK;
+    }
     int32_t* topk = outs && outs->topk_idx ? outs->topk_idx : reinterpret_cast<int32_t*>(ws + L.topk);
     float* gates = outs && outs->gates ? outs->gates : reinterpret_cast<float*>(ws + L.gates);
     int32_t* loads = outs->loads;
@@ -366,7 +374,7 @@ moe_status moe_layer_forward(const moe_layer_weights* w, const uint16_t* u, int6
                              moe_stream_t stream) {
     STATUS_OK(check_layer(w));
     REQUIRE(outs && outs->loads, "moe_layer_forward: outputs need a loads buffer");
-    REQUIRE(T >= 0 && u && out, "moe_layer_forward: null u/out");
+    REQUIRE(T >= 0 && (T == 0 || (u && out)), "moe_layer_forward: null u/out");
     const LayerWs L = layer_ws(w, T, false);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MOE_ERR_WORKSPACE, "moe_layer_forward: workspace needs %zu bytes, 256-byte aligned", L.total);
@@ -378,7 +386,7 @@ moe_status moe_layer_forward_host(const moe_layer_weights* w, const uint16_t* u_
                                   size_t workspace_bytes, moe_stream_t stream) {
     STATUS_OK(check_layer(w));
     REQUIRE(outs && outs->loads, "moe_layer_forward_host: outputs need a loads buffer");
-    REQUIRE(T >= 0 && u_host && out_host, "moe_layer_forward_host: null u/out");
+    REQUIRE(T >= 0 && (T == 0 || (u_host && out_host)), "moe_layer_forward_host: null u/out");
     const LayerWs L = layer_ws(w, T, true);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MOE_ERR_WORKSPACE, "moe_layer_forward_host: workspace needs %zu bytes", L.total);

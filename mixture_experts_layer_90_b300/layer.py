@@ -86,6 +86,9 @@ class MoELayer:
     def _outs(self, topk_idx, gates, events=None):
         self._ev_arr = None
         if events is not None:
+            for e in events:
+                if e.cuda_event == 0:      # torch creates the CUDA event on its first record
+                    e.record()
             self._ev_arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         return LayerOutputs(topk_idx=topk_idx.data_ptr() if topk_idx is not None else None,
                             gates=gates.data_ptr() if gates is not None else None,
