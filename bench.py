@@ -36,6 +36,25 @@ FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1
 KERNELS_PER_STEP = 11        # split, gate GEMM, select | count, scan, rank, scatter | GEMM1 | GEMM2 | combine | bias
 
 
+def profiled_traffic(name):
+    """DRAM bytes per launch of a kernel from its committed ncu summary
+    (profiles/traffic.md, lines `name: bytes sha1`), or None when the kernel
+    source changed since the counters were taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    h = hashlib.sha1()
+    for f in ("gemm.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_layer_90_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    for ln in open(p):
+        parts = ln.strip().strip("`").split()
+        if len(parts) == 3 and parts[0] == name + ":" and parts[2] == h.hexdigest()[:12]:
+            return float(parts[1])
+    return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -56,14 +75,19 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.start, self.stop = 0, None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 10.0 and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.start = len(self.lines)
         except OSError:
             self.proc = None
         return self
@@ -73,6 +97,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.stop = len(self.lines)
         if self.proc:
             self.proc.terminate()
             try:
@@ -83,7 +108,7 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[getattr(self, "start", 0):getattr(self, "stop", None)]:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -271,11 +296,7 @@ def run_ours(args):
     t2s = stage_ms["gemm2"] / 1000.0
     gemm1_tflops = g1 / t1s / 1e12
     gemm_pct = 100.0 * (g1 + g2) / (t1s + t2s) / 1e12 / fp8_peak
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
-    if os.path.exists(tp):
-        with open(tp) as f:
-            traffic = json.load(f).get("bytes_per_launch")
+    traffic = profiled_traffic("gemm1_swiglu")
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -300,7 +321,7 @@ def run_ours(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         inputs = (u_bufs[0].cpu(), cent.cpu(), bias.cpu(),
                   lambda e: tuple(w.cpu() for w in S.expert_weights(sh, e, device=dev)))
-        n = max(1, int(os.environ.get("CPU_BASELINE_TOKENS", "4")))
+        n = max(1, int(os.environ.get("CPU_BASELINE_TOKENS", "12")))
         v, dt, cores = oracle_sample_timing(sh, inputs, n, seed=99)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{n} tokens of the same workload ({dt:.1f} s): routing, FP8 "
@@ -311,16 +332,159 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# --------------------------------------------------------------------------
+# single-kernel workloads (the other configurations, and small profiling cases)
+# --------------------------------------------------------------------------
+
+class L2Flush:
+    """Writes a buffer twice the size of L2 so the next launch starts cold."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.buf = torch.empty(max(2 * l2, 1 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_launches(fn, steps, warmup, flush=None):
+    """Mean device time (ms) of fn() over `steps` launches, each bracketed by
+    CUDA events on the current stream, with an optional L2 flush before each."""
+    import torch
+    for _ in range(warmup):
+        if flush:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        if flush:
+            flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def grouped_fp8_operands(moe, S, dev, rows_per_group, G, Nd, Kd, seed=0):
+    """Row-grouped E4M3 activations [G*rows, Kd] and G weight matrices [Nd, Kd],
+    drawn N(0,1) and N(0, 1/sqrt(Kd)) and quantised by this library's kernels."""
+    import torch
+    M = rows_per_group * G
+    a = S.normal((M, Kd), 1.0, S.key(seed, "case-a", M, Kd), device=dev)
+    qa, sa = moe.fp8_quant_1x128(a)
+    del a
+    qb = torch.empty((G, Nd, Kd), dtype=torch.uint8, device=dev)
+    sb = torch.empty((G, Nd // 128, Kd // 128), dtype=torch.float32, device=dev)
+    for g in range(G):
+        w = S.normal((Nd, Kd), 1.0 / math.sqrt(Kd), S.key(seed, "case-b", g, Nd, Kd), device=dev)
+        moe.fp8_quant_128x128(w, qb[g], sb[g])
+    offs = torch.arange(0, M + 1, rows_per_group, dtype=torch.int32, device=dev)
+    return qa, sa, qb, sb, offs
+
+
+def run_case(args):
+    import torch
+
+    import mixture_experts_layer_90_b300 as moe
+    import synthetic as S
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pk, src = peaks()
+    flush = L2Flush(dev)
+    line = {"case": args.case, "steps": args.steps, "warmup": args.warmup, "data": "synthetic"}
+    if args.case in ("gemm", "gemm1-small", "gemm2-small"):
+        if args.case == "gemm":
+            cfg = S.GEMM_V3
+            a, b = S.gemm_operands(cfg["M"], cfg["K"], cfg["N"], device=dev)
+            qa, sa = moe.fp8_quant_1x128(a)
+            qb, sb = moe.fp8_quant_128x128(b)
+            qb, sb = qb[None], sb[None]
+            offs = torch.tensor([0, cfg["M"]], dtype=torch.int32, device=dev)
+            M, Nd, Kd, epi = cfg["M"], cfg["N"], cfg["K"], moe.MOE_EPI_BF16
+            workload = "fp8-gemm-4096x4096x7168"
+        else:
+            # one expert's average share of the V3 layer: 33 groups (32 routed + shared) of 256 rows
+            G, rows = 33, 256
+            Nd, Kd, epi = (4096, 7168, moe.MOE_EPI_SWIGLU_FP8) if args.case == "gemm1-small" else \
+                          (7168, 2048, moe.MOE_EPI_BF16)
+            qa, sa, qb, sb, offs = grouped_fp8_operands(moe, S, dev, rows, G, Nd, Kd)
+            M = G * rows
+            workload = f"grouped-fp8-{G}x{rows}x{Nd}x{Kd}"
+        outs = moe.fp8_grouped_gemm(qa, sa, qb, sb, offs, epi)
+        C, cs = outs if epi == moe.MOE_EPI_SWIGLU_FP8 else (outs, None)
+        ms = time_launches(lambda: moe.fp8_grouped_gemm(qa, sa, qb, sb, offs, epi, C=C, c_scales=cs),
+                           args.steps, args.warmup, flush)
+        assert moe.device_status() == 0
+        flop = 2.0 * M * Nd * Kd
+        fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
+        line.update(workload=workload, ms=ms, tflops=flop / ms / 1e9,
+                    frac_of_fp8_peak=flop / ms / 1e9 / fp8_peak,
+                    peak_source=f"{src} bf16 burst x {FP8_OVER_BF16}", l2="flushed before each launch")
+    elif args.case == "route":
+        sh = S.ROUTE_V3
+        u = S.tokens(sh, device=dev)
+        cent = S.centroids(sh, device=dev)
+        bias = S.bias(sh, device=dev)
+        T, d, N, K = sh.T, sh.d, sh.N, sh.K
+        L = moe.load_library()
+        ws_r = moe._ws(L.moe_route_workspace_size(T, d, N, moe.MOE_DTYPE_F32), dev)
+        ws_p = moe._ws(L.moe_permute_workspace_size(T, N), dev)
+        idx, gates, loads, _ = moe.moe_route(u, cent, bias, K, workspace=ws_r)
+        off, perm, dest, xp, _ = moe.moe_permute(u, idx, N, workspace=ws_p)
+
+        def step():
+            moe.moe_route(u, cent, bias, K, workspace=ws_r)
+            moe.moe_permute(u, idx, N, workspace=ws_p)
+            moe.moe_bias_update(bias, loads, T, K, sh.gamma)
+        ms = time_launches(step, args.steps, args.warmup, flush)
+        ms_route = time_launches(lambda: moe.moe_route(u, cent, bias, K, workspace=ws_r), args.steps,
+                                 args.warmup, flush)
+        ms_perm = time_launches(lambda: moe.moe_permute(u, idx, N, workspace=ws_p), args.steps, args.warmup, flush)
+        assert moe.device_status() == 0
+        # algorithmic bytes: u read twice (gate, scatter), centroids, bias, the K bf16 copies written,
+        # indices / gates / rows / tokens (int32 or fp32) written
+        alg = 2 * T * d * 2 + N * d * 4 + T * K * d * 2 + T * K * 4 * 4 + N * 12
+        line.update(workload="route-dispatch-16384x7168-256e-top8", ms=ms, tokens_per_s=T / ms * 1e3,
+                    gbs=alg / ms / 1e6, frac_of_hbm=alg / ms / 1e6 / pk["hbm_gbs"], ms_route=ms_route,
+                    ms_permute=ms_perm, permute_gbs=(T * d * 2 + T * K * d * 2 + T * K * 12) / ms_perm / 1e6,
+                    algorithmic_bytes=alg, l2="flushed before each step")
+    elif args.case in ("decode64", "decode256"):
+        sh = S.DECODE_V3[0 if args.case == "decode64" else 1]
+        cent = S.centroids(sh, zipf=True).to(dev)
+        bias = S.bias(sh).to(dev)
+        layer = moe.MoELayer.build(sh.d, sh.N, sh.K, sh.I, cent, bias,
+                                   lambda e: S.expert_weights(sh, e, device=dev), fp8=True, gamma=sh.gamma,
+                                   n_groups=sh.n_groups, topk_groups=sh.topk_groups)
+        u = S.tokens(sh, seed=3, device=dev)
+        out = torch.empty_like(u)
+        ms = time_launches(lambda: layer.forward(u, out, update_bias=False), args.steps, args.warmup, flush)
+        assert moe.device_status() == 0
+        active = int((layer.loads > 0).sum().item()) + 1
+        per_expert = 3 * sh.I * sh.d + 4 * (3 * sh.I * sh.d // 16384)
+        alg = active * per_expert + 2 * sh.T * sh.d * 2
+        line.update(workload=sh.name, ms=ms, tokens_per_s=sh.T / ms * 1e3, active_experts=active,
+                    gbs=alg / ms / 1e6, frac_of_hbm=alg / ms / 1e6 / pk["hbm_gbs"], l2="flushed before each step")
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="layer",
+                    choices=["layer", "gemm", "gemm1-small", "gemm2-small", "route", "decode64", "decode256"],
+                    help="layer: the V3 layer step (the benchmark line); the others time one workload alone")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.case != "layer":
+        run_case(args)
     else:
         run_ours(args)
 
