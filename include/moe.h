@@ -19,7 +19,8 @@
  *   - All tensor pointers are DEVICE memory owned by the caller, except in
  *     moe_layer_forward_host, whose u/out are host memory. The library never
  *     allocates or frees device memory; scratch comes from a caller workspace
- *     sized by the matching *_workspace_size function.
+ *     sized by the matching *_workspace_size function (moe_permute_static
+ *     instead uses a fixed array inside the library, see there).
  *   - Calls are asynchronous on `stream` and return synchronously checked
  *     argument errors. Device-side problems (a pipeline wait that ran out of
  *     time, inconsistent group offsets) set a device status word that
@@ -131,6 +132,31 @@ moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_
                        int out_dtype, int with_shared, int32_t* offsets, int32_t* perm_token,
                        int32_t* dest_row, void* x_perm, float* x_perm_scales,
                        void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_permute without a workspace. The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory, such as code
+ * whose device memory all belongs to another allocator it cannot ask for a
+ * buffer, or code that must not allocate once running (cudaMalloc can
+ * synchronise the device or fail under memory pressure).
+ *
+ * Same arguments, outputs and rules as moe_permute. The scratch (per-chunk
+ * expert histograms) is a 4 MiB array inside the library, held on every GPU
+ * that loads the library until the process exits. Limit: ceil(T/32)*N + N
+ * <= 1,048,576 (e.g. N = 256 allows T <= 131,040); larger sizes return
+ * MOE_ERR_WORKSPACE without launching anything. Calls no allocator.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress) and caches it. Make that first call
+ * before any stream capture.
+ *
+ * Every call on a device shares the one array. The kernels write each
+ * scratch entry before reading it, so nothing must start at zero and the
+ * previous call's contents do not matter. Calls that overlap on the GPU
+ * (different streams, no ordering between them) race on the array and give
+ * wrong results: order them on one stream, or use moe_permute. */
+moe_status moe_permute_static(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K,
+                              int out_dtype, int with_shared, int32_t* offsets, int32_t* perm_token,
+                              int32_t* dest_row, void* x_perm, float* x_perm_scales, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Grouped GEMMs — learn.ifs.name summary, paragraphs on FP8 tiles and on     */

@@ -25,7 +25,7 @@ EXPORTS = [
     "moe_last_error", "moe_num_sms", "moe_get_device_status",
     "fp8_quant_1x128", "fp8_quant_128x128",
     "moe_route_workspace_size", "moe_route",
-    "moe_permute_workspace_size", "moe_permute",
+    "moe_permute_workspace_size", "moe_permute", "moe_permute_static",
     "fp8_grouped_gemm", "bf16_grouped_gemm",
     "moe_combine", "moe_bias_update",
     "moe_layer_workspace_size", "moe_layer_forward",
@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_route": (i32, [vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
         "moe_permute_workspace_size": (sz, [i64, i32]),
         "moe_permute": (i32, [vp, i64, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "moe_permute_static": (i32, [vp, i64, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
         "fp8_grouped_gemm": (i32, [vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, vp, vp]),
         "bf16_grouped_gemm": (i32, [vp, vp, vp, i32, i64, i32, i32, i32, vp, vp]),
         "moe_combine": (i32, [vp, vp, vp, vp, vp, i64, i32, i32, i64, vp, vp]),
@@ -195,6 +196,26 @@ def moe_permute(x, topk_idx, N, out_dtype=MOE_DTYPE_BF16, with_shared=False, wor
     ws = _ws(need, dev) if workspace is None else workspace
     _check(L.moe_permute(_p(x), T, d, _p(topk_idx), N, K, out_dtype, int(bool(with_shared)), _p(offsets), _p(perm),
                          _p(dest), _p(xp), _p(xs), _p(ws), ws.numel(), _stream()), "moe_permute")
+    return offsets, perm, dest, xp, xs
+
+
+def moe_permute_static(x, topk_idx, N, out_dtype=MOE_DTYPE_BF16, with_shared=False):
+    """moe_permute without a workspace: its scratch is a fixed array inside the
+    library (for callers that cannot allocate device memory). Same outputs."""
+    _require_cuda()
+    L = load_library()
+    T, d = x.shape
+    K = topk_idx.shape[1]
+    dev = x.device
+    R = T * K + (T if with_shared else 0)
+    offsets = torch.empty((N + 1 + (1 if with_shared else 0),), dtype=torch.int32, device=dev)
+    perm = torch.empty((T * K,), dtype=torch.int32, device=dev)
+    dest = torch.empty((T, K), dtype=torch.int32, device=dev)
+    fp8 = out_dtype == MOE_DTYPE_E4M3
+    xp = torch.empty((R, d), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    xs = torch.empty((d // 128, R), dtype=torch.float32, device=dev) if fp8 else None
+    _check(L.moe_permute_static(_p(x), T, d, _p(topk_idx), N, K, out_dtype, int(bool(with_shared)), _p(offsets),
+                                _p(perm), _p(dest), _p(xp), _p(xs), _stream()), "moe_permute_static")
     return offsets, perm, dest, xp, xs
 
 

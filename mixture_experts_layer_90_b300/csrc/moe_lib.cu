@@ -5,5 +5,6 @@
 #include "combine.cu"
 #include "gemm.cu"
 #include "permute.cu"
+#include "permute_static.cu"
 #include "quant.cu"
 #include "route.cu"
