@@ -13,7 +13,10 @@
 // Block roles (576 threads):
 //   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and, in
 //               warpgroup w/4, the columns {32*(w/4) + c} and {128 + 32*(w/4) + c};
-//   warp 16     TMA producer (one elected lane);
+//   warp 16     producer: one lane issues the TMA tile loads; for FP8 all 32
+//               lanes also copy each K block's 128 row scales and 2 weight
+//               scales into a shared-memory ring (cp.async), so the epilogue
+//               never waits on a global load inside its promotion loop;
 //   warp 17     tcgen05.mma issuer (one elected lane) + TMEM owner.
 // Tile: 128 rows x 256 columns, K step 128 bytes (128 e4m3 or 64 bf16),
 // 4-stage shared-memory ring (48 KB per stage), 2 x 256 TMEM columns.
@@ -30,14 +33,22 @@ constexpr int kABytes = kBM * 128, kBBytes = kBN * 128;
 constexpr int kEpiWarps = 16, kThreads = (kEpiWarps + 2) * 32;
 constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
 constexpr int kMaxGroups = 1024;
+constexpr int kSSlots = 8;   // K blocks of scales staged ahead of the epilogue
+
+struct ScaleSlot {
+    float sa[kBM];   // activation scale of each row of the tile, this K block
+    float sb[4];     // weight scales of the tile's two 128-column blocks (+ pad)
+};
 
 struct Smem {
     uint64_t full[kStages], empty[kStages];
+    uint64_t sfull[kSSlots], sempty[kSSlots];
     uint64_t tfull[2], tempty[2], xchg[2], drain;
     uint32_t tmem_base;
     int abort;
     int total_items;
     float amax[2][4][128];
+    ScaleSlot scales[kSSlots];
     int prefix[kMaxGroups + 1];
     int offs[kMaxGroups + 1];
 };
@@ -90,6 +101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(&s.full[i]), 1);
             mbar_init(smem_u32(&s.empty[i]), 1);
+        }
+        for (int i = 0; i < kSSlots; ++i) {
+            mbar_init(smem_u32(&s.sfull[i]), 32);         // one cp.async arrival per producer lane
+            mbar_init(smem_u32(&s.sempty[i]), kEpiWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s.tfull[i]), 1);
@@ -150,40 +165,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = s.total_items;
 
     if (warp == kProducerWarp) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int armed[kStages] = {0, 0, 0, 0};
-            for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
-                Item it = decode(item, s, G, n_tiles_n, splits);
-                const int a_row = s.offs[it.g] + it.mt * kBM;
-                const int b_row = it.g * args.Nd + it.nt * kBN;
-                const int k0 = it.sp * steps_per_split;
-                const int k1 = min(args.k_steps, k0 + steps_per_split);
-                bool ok = true;
-                for (int ks = k0; ks < k1; ++ks) {
-                    if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort)) {
-                        ok = false;
-                        break;
+        // ---------------- producer: TMA tiles (lane 0), FP8 scales (all lanes) ----------------
+        int stage = 0, sslot = 0;
+        uint32_t phase = 0, sphase = 0;
+        int armed[kStages] = {0, 0, 0, 0};
+        const int nkb = args.Kd / 128;
+        bool stop = false;
+        for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+            Item it = decode(item, s, G, n_tiles_n, splits);
+            const int a_row = s.offs[it.g] + it.mt * kBM;
+            const int b_row = it.g * args.Nd + it.nt * kBN;
+            const int k0 = it.sp * steps_per_split;
+            const int k1 = min(args.k_steps, k0 + steps_per_split);
+            // this lane copies the scales of rows a_row + 4*lane .. +3 (clamped into the matrix:
+            // rows past a group's end are computed but never stored)
+            const float* sa_src[4];
+            const float* sb_src = nullptr;
+            if (kMode == kModeFP8) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t r = min(int64_t(a_row) + 4 * lane + i, args.M_total - 1);
+                    sa_src[i] = args.sa + r;
+                }
+                sb_src = args.sb + (int64_t(it.g) * (args.Nd / 128) + 2 * it.nt) * nkb;
+            }
+            for (int ks = k0; ks < k1; ++ks) {
+                int ok = 1;
+                if (lane == 0) {
+                    if (kMode == kModeFP8) ok = mbar_wait(smem_u32(&s.sempty[sslot]), sphase ^ 1u, abort);
+                    if (ok) ok = mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    stop = true;
+                    break;
+                }
+                if (kMode == kModeFP8) {
+                    const int64_t koff = int64_t(ks) * args.lda_s;
+                    const uint32_t dst = smem_u32(&s.scales[sslot].sa[4 * lane]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) cp_async_4(dst + 4 * i, sa_src[i] + koff);
+                    if (lane == 0) {
+                        cp_async_4(smem_u32(&s.scales[sslot].sb[0]), sb_src + ks);
+                        cp_async_4(smem_u32(&s.scales[sslot].sb[1]), sb_src + nkb + ks);
                     }
+                    cp_async_arrive_noinc(smem_u32(&s.sfull[sslot]));
+                    if (++sslot == kSSlots) {
+                        sslot = 0;
+                        sphase ^= 1u;
+                    }
+                }
+                if (lane == 0) {
                     const uint32_t fb = smem_u32(&s.full[stage]);
                     mbar_arrive_expect_tx(fb, kABytes + kBBytes);
                     tma_load_2d(ringA + stage * kABytes, &tmA, fb, (ks % args.a_k_steps) * args.elems_per_step,
                                 a_row);
                     tma_load_2d(ringB + stage * kBBytes, &tmB, fb, ks * args.elems_per_step, b_row);
                     armed[stage] += 1;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                 }
-                if (!ok) break;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            // never leave the block while a copy into its shared memory is in flight
+        }
+        // never leave the block while a copy into its shared memory is in flight
+        if (kMode == kModeFP8) cp_async_wait_all();
+        if (lane == 0)
             for (int i = 0; i < kStages; ++i)
                 if (armed[i] > 0) mbar_wait_limit(smem_u32(&s.full[i]), uint32_t(armed[i] - 1) & 1u, 200000000ull);
-        }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ---------------- tcgen05.mma issuer ----------------
@@ -254,33 +304,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = tmem_base + (uint32_t(q * 32) << 16);
         uint32_t acc_iter = 0, tile_iter = 0;
+        int sslot = 0;
+        uint32_t sphase = 0;
         for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
-            Item it = decode(item, s, G, n_tiles_n, splits);
-            const int k0 = it.sp * steps_per_split;
-            const int k1 = min(args.k_steps, k0 + steps_per_split);
-            const int rows_g = s.offs[it.g + 1] - s.offs[it.g];
-            const int row_local = it.mt * kBM + row_in_tile;
-            const bool valid = row_local < rows_g;
-            const int64_t grow = int64_t(s.offs[it.g]) + row_local;
+            int k0, k1;
+            {
+                const Item it = decode(item, s, G, n_tiles_n, splits);
+                k0 = it.sp * steps_per_split;
+                k1 = min(args.k_steps, k0 + steps_per_split);
+            }
             float acc[64];
             bool ok = true;
             if (kMode == kModeFP8) {
+                // promotion (accumulation paragraph): each 128-K block's partial sums,
+                // times sa[row, kb] * sb[nblk, kb], added into fp32 registers
+                float2 acc2[32];
 #pragma unroll
-                for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-                const int nkb = args.Kd / 128;
-                const float* sb_lo = args.sb + (int64_t(it.g) * (args.Nd / 128) + 2 * it.nt) * nkb;
-                // rows past the group's end read row 0's scale (never stored)
-                const float* sa_p = args.sa + (valid ? grow : 0) + int64_t(k0) * args.lda_s;
-                const uint32_t lda = uint32_t(args.lda_s);
-                float sa0 = __ldg(sa_p);
-                float fl_n = sa0 * __ldg(sb_lo + k0), fh_n = sa0 * __ldg(sb_lo + nkb + k0);
+                for (int i = 0; i < 32; ++i) acc2[i] = make_float2(0.0f, 0.0f);
                 for (int ks = k0; ks < k1; ++ks) {
-                    const float fl = fl_n, fh = fh_n;
-                    if (ks + 1 < k1) {
-                        sa_p += lda;
-                        const float sa1 = __ldg(sa_p);
-                        fl_n = sa1 * __ldg(sb_lo + ks + 1);
-                        fh_n = sa1 * __ldg(sb_lo + nkb + ks + 1);
+                    if (!mbar_wait(smem_u32(&s.sfull[sslot]), sphase, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const float sa_v = s.scales[sslot].sa[row_in_tile];
+                    const float fl = sa_v * s.scales[sslot].sb[0];
+                    const float fh = sa_v * s.scales[sslot].sb[1];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&s.sempty[sslot]));
+                    if (++sslot == kSSlots) {
+                        sslot = 0;
+                        sphase ^= 1u;
                     }
                     const uint32_t buf = acc_iter & 1u;
                     if (!mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort)) {
@@ -302,10 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
                         }
                         const float f = c < 2 ? fl : fh;
+                        const float2 f2 = make_float2(f, f);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[c * 16 + i] = fmaf(__uint_as_float(r[i]), f, acc[c * 16 + i]);
+                        for (int i = 0; i < 8; ++i)
+                            acc2[c * 8 + i] = __ffma2_rn(
+                                make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), f2,
+                                acc2[c * 8 + i]);
                     }
                     acc_iter += 1;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    acc[2 * i] = acc2[i].x;
+                    acc[2 * i + 1] = acc2[i].y;
                 }
             } else {
                 const uint32_t buf = tile_iter & 1u;
@@ -327,7 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
 
-            // ---- epilogue of the tile ----
+            // ---- epilogue of the tile (tile coordinates decoded again: fewer live registers) ----
+            const Item it = decode(item, s, G, n_tiles_n, splits);
+            const int row_local = it.mt * kBM + row_in_tile;
+            const bool valid = row_local < s.offs[it.g + 1] - s.offs[it.g];
+            const int64_t grow = int64_t(s.offs[it.g]) + row_local;
             constexpr int ep = kEpi;
             if constexpr (ep == MOE_EPI_SWIGLU_FP8 || ep == MOE_EPI_SWIGLU_BF16) {
                 float a[32];
