@@ -29,7 +29,8 @@
  *     scales as fp32. Row-major unless stated.
  *   - Activation scales are stored K-block-major: scales[kb * ld + row]
  *     (kb = column / 128). Weight scales are [rows/128][cols/128] row-major.
- *   - Pointers used by vector or TMA loads must be 16-byte aligned.
+ *   - Pointers used by vector or TMA loads must be 16-byte aligned; GEMM
+ *     outputs (C) 32-byte aligned.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H

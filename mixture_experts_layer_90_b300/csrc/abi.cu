@@ -37,6 +37,7 @@ moe_status fail(moe_status st, const char* fmt, ...) {
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool al8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+bool al32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 #define REQUIRE(cond, ...)                                    \
@@ -176,7 +177,7 @@ moe_status fp8_grouped_gemm(const uint8_t* A, const float* sa, const uint8_t* B,
     if (M_total == 0) return MOE_OK;
     REQUIRE(A && sa && C, "fp8_grouped_gemm: null pointer");
     REQUIRE(epilogue != MOE_EPI_SWIGLU_FP8 || c_scales, "fp8_grouped_gemm: SwiGLU output needs scales");
-    REQUIRE(al16(A) && al16(C), "fp8_grouped_gemm: A and C must be 16-byte aligned");
+    REQUIRE(al16(A) && al32(C), "fp8_grouped_gemm: A must be 16-byte and C 32-byte aligned");
     CUtensorMap ta, tb;
     if (!moe::make_kmajor_map(&ta, A, false, uint64_t(Kd), uint64_t(M_total), uint64_t(Kd), 128) ||
         !moe::make_kmajor_map(&tb, B, false, uint64_t(Kd), uint64_t(G) * Nd, uint64_t(Kd), 256))
@@ -214,7 +215,7 @@ moe_status bf16_grouped_gemm(const uint16_t* A, const uint16_t* B, const int32_t
     REQUIRE(al16(B), "bf16_grouped_gemm: B must be 16-byte aligned");
     if (M_total == 0) return MOE_OK;
     REQUIRE(A && C, "bf16_grouped_gemm: null pointer");
-    REQUIRE(al16(A) && al16(C), "bf16_grouped_gemm: A and C must be 16-byte aligned");
+    REQUIRE(al16(A) && al32(C), "bf16_grouped_gemm: A must be 16-byte and C 32-byte aligned");
     CUtensorMap ta, tb;
     if (!moe::make_kmajor_map(&ta, A, true, uint64_t(Kd), uint64_t(M_total), uint64_t(Kd) * 2, 128) ||
         !moe::make_kmajor_map(&tb, B, true, uint64_t(Kd), uint64_t(G) * Nd, uint64_t(Kd) * 2, 256))
