@@ -230,6 +230,7 @@ moe_status bf16_grouped_gemm(const uint16_t* A, const uint16_t* B, const int32_t
     a.a_k_steps = Kd / 64;
     a.elems_per_step = 64;
     a.splits = 1;
+    a.promote_steps = moe::kBf16PromoteSteps;
     a.epilogue = epilogue;
     a.C = C;
     CUDA_OK(moe::run_grouped_gemm(moe::kModeBF16, ta, tb, a, moe::num_sms(), stream));

@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ---------------- tcgen05.mma issuer ----------------
         constexpr uint32_t idesc = kMode == kModeFP8 ? make_idesc(0, 0, kBM, kBN) : make_idesc(1, 1, kBM, kBN);
+        const int P = kMode == kModeFP8 ? 1 : args.promote_steps;
         int stage = 0;
         uint32_t phase = 0;
         uint32_t acc_iter = 0;
@@ -256,12 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k1 = min(args.k_steps, k0 + steps_per_split);
             uint32_t buf = acc_iter & 1u;
             bool ok = true;
-            if (kMode != kModeFP8) {
-                if (!mbar_wait(smem_u32(&s.tempty[buf]), ((acc_iter >> 1) & 1u) ^ 1u, abort)) break;
-                tc_fence_after();
-            }
             for (int ks = k0; ks < k1; ++ks) {
-                if (kMode == kModeFP8) {
+                // one TMEM partial per chunk of P K steps (FP8: every 128-K block)
+                const bool first = (ks - k0) % P == 0;
+                const bool last = (ks - k0) % P == P - 1 || ks == k1 - 1;
+                if (first) {
                     buf = acc_iter & 1u;
                     if (!mbar_wait(smem_u32(&s.tempty[buf]), ((acc_iter >> 1) & 1u) ^ 1u, abort)) {
                         ok = false;
@@ -279,26 +279,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t d = tmem_base + buf * kBN;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint32_t acc = (k > 0 || (kMode != kModeFP8 && ks > k0)) ? 1u : 0u;
+                        const uint32_t acc = (k > 0 || !first) ? 1u : 0u;
                         if (kMode == kModeFP8) mma_e4m3(d, ad + 2 * k, bd + 2 * k, idesc, acc);
                         else mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, acc);
                     }
                     tc_commit(smem_u32(&s.empty[stage]));
-                    if (kMode == kModeFP8) tc_commit(smem_u32(&s.tfull[buf]));
+                    if (last) tc_commit(smem_u32(&s.tfull[buf]));
                 }
                 __syncwarp();
-                if (kMode == kModeFP8) acc_iter += 1;
+                if (last) acc_iter += 1;
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            if (kMode != kModeFP8) {
-                if (lane == 0) tc_commit(smem_u32(&s.tfull[buf]));
-                __syncwarp();
-                acc_iter += 1;
-            }
         }
         // every issued MMA must be complete before TMEM is freed
         if (lane == 0) {
@@ -379,21 +374,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc[2 * i + 1] = acc2[i].y;
                 }
             } else {
-                const uint32_t buf = tile_iter & 1u;
-                if (!mbar_wait(smem_u32(&s.tfull[buf]), (tile_iter >> 1) & 1u, abort)) break;
-                tc_fence_after();
-                const uint32_t col = lane_addr + buf * kBN + wg * 32;
-                uint32_t r0[32], r1[32];
-                tmem_ld_32(col, r0);
-                tmem_ld_32(col + 128, r1);
-                tmem_wait_ld(r0, r1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+                // bf16: the partial sums of each chunk of P K steps are added into fp32
+                // registers (fp32 accumulation in TMEM over at most P * 64 products)
+                const int P = args.promote_steps;
+                float2 acc2[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+                for (int c0 = k0; c0 < k1; c0 += P) {
+                    const uint32_t buf = acc_iter & 1u;
+                    if (!mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t col = lane_addr + buf * kBN + wg * 32;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[16];
+                        tmem_ld_16(col + (c >> 1) * 128 + (c & 1) * 16, r);
+                        tmem_wait_ld(r);
+                        if (c == 3) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            acc2[c * 8 + i] = __fadd2_rn(
+                                acc2[c * 8 + i], make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])));
+                    }
+                    acc_iter += 1;
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    acc[i] = __uint_as_float(r0[i]);
-                    acc[32 + i] = __uint_as_float(r1[i]);
+                    acc[2 * i] = acc2[i].x;
+                    acc[2 * i + 1] = acc2[i].y;
                 }
             }
             if (!ok) break;

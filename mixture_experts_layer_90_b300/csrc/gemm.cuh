@@ -9,6 +9,11 @@ namespace moe {
 
 enum { kModeFP8 = 0, kModeBF16 = 1 };
 
+// bf16 GEMMs add their TMEM partial sums into fp32 registers every this many
+// 64-wide K steps (512 products): a long fp32 accumulation in the tensor
+// cores alone drifts by ~1e-5 relative over the 21,504-term routing gate.
+constexpr int kBf16PromoteSteps = 8;
+
 struct GemmArgs {
     const int32_t* group_offsets;  // [G+1] device; nullptr = one group of M_total rows
     int G;
@@ -19,6 +24,7 @@ struct GemmArgs {
     int a_k_steps;       // A's K extent in steps; A's step = step % a_k_steps
     int elems_per_step;  // 128 (e4m3) or 64 (bf16)
     int splits;          // split-K parts (MOE_EPI_F32 only; else 1)
+    int promote_steps;   // bf16: K steps accumulated in TMEM before adding into fp32 registers
     int epilogue;        // MOE_EPI_*
     const float* sa;     // FP8: [Kd/128][lda_s] activation scales
     int64_t lda_s;

@@ -218,15 +218,20 @@ RoutePlan plan_route(int64_t T, int d, int N, int centroid_dtype) {
     const int64_t k_steps = int64_t(p.terms) * d / 64;
     const int64_t base = (T + 127) / 128 * (p.n_pad / 256);
     const int sms = num_sms();
+    // Split-K count minimising (waves of tiles) x (K steps per tile) x (time of one
+    // K step) + (fp32 partial logits each split writes and the selection reads back).
+    // Constants: a 128 x 256 x 64 bf16 K step moves 48 KB and takes about 0.5 us on
+    // one SM; partials cost 8 bytes per logit per split at about 6 TB/s.
+    constexpr double kStepUs = 0.5, kBytesPerUs = 6.0e6;
     int best = 1;
     double best_cost = 1e300;
-    for (int sp = 1; sp <= 16 && sp <= k_steps; ++sp) {
+    for (int sp = 1; sp <= 64 && sp <= k_steps; ++sp) {
         if ((sp - 1) * ((k_steps + sp - 1) / sp) >= k_steps) continue;   // every split must get K steps
         const int64_t items = base * sp;
         const double waves = double((items + sms - 1) / sms);
         const double steps = double((k_steps + sp - 1) / sp);
-        // partial logits cost extra traffic: charge ~2% of a K step per split
-        const double cost = waves * steps + 0.02 * k_steps * (sp - 1) / 16.0;
+        const double partial_us = double(sp) * double(T) * p.n_pad * 8.0 / kBytesPerUs;
+        const double cost = waves * steps * kStepUs + partial_us;
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
             best = sp;
@@ -270,6 +275,7 @@ cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* centro
     a.a_k_steps = d / 64;
     a.elems_per_step = 64;
     a.splits = plan.splits;
+    a.promote_steps = kBf16PromoteSteps;
     a.epilogue = MOE_EPI_F32;
     a.C = zpart;
     const int64_t items = (T + 127) / 128 * (plan.n_pad / 256) * plan.splits;
