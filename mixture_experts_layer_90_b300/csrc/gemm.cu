@@ -10,14 +10,16 @@
 //   * bf16 expert GEMMs (FP32 accumulation over the whole K in TMEM).
 //   * the gate logits of routing (bf16, split-K partial sums in fp32).
 //
-// Block roles (576 threads):
+// Block roles (608 threads):
 //   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and, in
 //               warpgroup w/4, the columns {32*(w/4) + c} and {128 + 32*(w/4) + c};
-//   warp 16     producer: one lane issues the TMA tile loads; for FP8 all 32
-//               lanes also copy each K block's 128 row scales and 2 weight
-//               scales into a shared-memory ring (cp.async), so the epilogue
-//               never waits on a global load inside its promotion loop;
-//   warp 17     tcgen05.mma issuer (one elected lane) + TMEM owner.
+//   warp 16     TMA producer: one lane issues the tile loads and does nothing
+//               else (any other work in its loop delays the loads, and the
+//               tile feed is what bounds this kernel);
+//   warp 17     tcgen05.mma issuer (one elected lane) + TMEM owner;
+//   warp 18     FP8 scales: each K block's 128 row scales and 2 weight scales
+//               copied into a shared-memory ring (cp.async), so the epilogue
+//               never waits on a global load inside its promotion loop.
 // Tile: 128 rows x 256 columns, K step 128 bytes (128 e4m3 or 64 bf16),
 // 4-stage shared-memory ring (48 KB per stage), 2 x 256 TMEM columns.
 #include "common.cuh"
@@ -30,8 +32,8 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kBM = 128, kBN = 256;
 constexpr int kABytes = kBM * 128, kBBytes = kBN * 128;
-constexpr int kEpiWarps = 16, kThreads = (kEpiWarps + 2) * 32;
-constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+constexpr int kEpiWarps = 16, kThreads = (kEpiWarps + 3) * 32;
+constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1, kScaleWarp = kEpiWarps + 2;
 constexpr int kMaxGroups = 1024;
 constexpr int kSSlots = 8;   // K blocks of scales staged ahead of the epilogue
 
@@ -174,42 +176,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = s.total_items;
 
     if (warp == kProducerWarp) {
-        // ---------------- producer: TMA tiles (lane 0), FP8 scales (all lanes) ----------------
-        int stage = 0, sslot = 0;
-        uint32_t phase = 0, sphase = 0;
-        int armed[kStages] = {0, 0, 0, 0};
-        const int nkb = args.Kd / 128;
-        bool stop = false;
-        for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
-            Item it = decode(item, s, G, n_tiles_n, splits);
-            const int a_row = s.offs[it.g] + it.mt * kBM;
-            const int b_row = it.g * args.Nd + it.nt * kBN;
-            const int k0 = it.sp * steps_per_split;
-            const int k1 = min(args.k_steps, k0 + steps_per_split);
-            // this lane copies the scales of rows a_row + 4*lane .. +3 (clamped into the matrix:
-            // rows past a group's end are computed but never stored)
-            const float* sa_src[4];
-            const float* sb_src = nullptr;
-            if (kMode == kModeFP8) {
+        // ---------------- TMA producer: one lane, nothing else in its loop ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int armed[kStages] = {0, 0, 0, 0};
+            bool stop = false;
+            for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+                const Item it = decode(item, s, G, n_tiles_n, splits);
+                const int a_row = s.offs[it.g] + it.mt * kBM;
+                const int b_row = it.g * args.Nd + it.nt * kBN;
+                const int k0 = it.sp * steps_per_split;
+                const int k1 = min(args.k_steps, k0 + steps_per_split);
+                int ka = k0 % args.a_k_steps;   // A's K step (A wraps around for the split routing gate)
+                for (int ks = k0; ks < k1; ++ks) {
+                    if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&s.full[stage]);
+                    mbar_arrive_expect_tx(fb, kABytes + kBBytes);
+                    tma_load_2d(ringA + stage * kABytes, &tmA, fb, ka * args.elems_per_step, a_row);
+                    tma_load_2d(ringB + stage * kBBytes, &tmB, fb, ks * args.elems_per_step, b_row);
+                    armed[stage] += 1;
+                    if (++ka == args.a_k_steps) ka = 0;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // never leave the block while a copy into its shared memory is in flight
+            for (int i = 0; i < kStages; ++i)
+                if (armed[i] > 0) mbar_wait_limit(smem_u32(&s.full[i]), uint32_t(armed[i] - 1) & 1u, 200000000ull);
+        }
+        __syncwarp();
+    } else if (warp == kScaleWarp) {
+        // ---------------- FP8 scales: each K block's 128 row scales and 2 weight scales ----------------
+        // copied into the shared ring by all 32 lanes (cp.async), ahead of the epilogue
+        if (kMode == kModeFP8) {
+            int sslot = 0;
+            uint32_t sphase = 0;
+            const int nkb = args.Kd / 128;
+            bool stop = false;
+            for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+                const Item it = decode(item, s, G, n_tiles_n, splits);
+                const int a_row = s.offs[it.g] + it.mt * kBM;
+                // rows past a group's end are clamped into the matrix: computed, never stored
+                const float* sa_src[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int64_t r = min(int64_t(a_row) + 4 * lane + i, args.M_total - 1);
                     sa_src[i] = args.sa + r;
                 }
-                sb_src = args.sb + (int64_t(it.g) * (args.Nd / 128) + 2 * it.nt) * nkb;
-            }
-            for (int ks = k0; ks < k1; ++ks) {
-                int ok = 1;
-                if (lane == 0) {
-                    if (kMode == kModeFP8) ok = mbar_wait(smem_u32(&s.sempty[sslot]), sphase ^ 1u, abort);
-                    if (ok) ok = mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    stop = true;
-                    break;
-                }
-                if (kMode == kModeFP8) {
+                const float* sb_src = args.sb + (int64_t(it.g) * (args.Nd / 128) + 2 * it.nt) * nkb;
+                for (int ks = 0; ks < nkb; ++ks) {
+                    int ok = 1;
+                    if (lane == 0) ok = mbar_wait(smem_u32(&s.sempty[sslot]), sphase ^ 1u, abort);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        stop = true;
+                        break;
+                    }
                     const int64_t koff = int64_t(ks) * args.lda_s;
                     const uint32_t dst = smem_u32(&s.scales[sslot].sa[4 * lane]);
 #pragma unroll
@@ -224,25 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sphase ^= 1u;
                     }
                 }
-                if (lane == 0) {
-                    const uint32_t fb = smem_u32(&s.full[stage]);
-                    mbar_arrive_expect_tx(fb, kABytes + kBBytes);
-                    tma_load_2d(ringA + stage * kABytes, &tmA, fb, (ks % args.a_k_steps) * args.elems_per_step,
-                                a_row);
-                    tma_load_2d(ringB + stage * kBBytes, &tmB, fb, ks * args.elems_per_step, b_row);
-                    armed[stage] += 1;
-                }
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
+            cp_async_wait_all();   // no copy into shared memory may outlive the block
         }
-        // never leave the block while a copy into its shared memory is in flight
-        if (kMode == kModeFP8) cp_async_wait_all();
-        if (lane == 0)
-            for (int i = 0; i < kStages; ++i)
-                if (armed[i] > 0) mbar_wait_limit(smem_u32(&s.full[i]), uint32_t(armed[i] - 1) & 1u, 200000000ull);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ---------------- tcgen05.mma issuer ----------------
