@@ -262,6 +262,23 @@ moe_status moe_layer_forward_host(const moe_layer_weights* w, const uint16_t* u_
                                   uint16_t* out_host, const moe_layer_outputs* outs, int update_bias,
                                   void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* Pipelined form of moe_layer_forward_host for a stream of batches: the
+ * host-to-device copy of one call and the device-to-host copy of the previous
+ * call run on two copy streams of the library while a call computes on
+ * `stream`, so copies and compute of consecutive calls overlap.
+ * Alternate `slot` (0, 1, 0, 1, ...) between consecutive calls that share one
+ * workspace (sized by moe_layer_host_pipeline_workspace_size, same w and T).
+ * `done_event` (a cudaEvent_t the caller created) is recorded once h' is in
+ * out_host; a synchronisation of `stream` alone does NOT cover that copy.
+ * out_host may be read, and u_host overwritten, once `done_event` has
+ * completed. The copy streams and events are created on the first call on a
+ * device and live until the process exits. */
+size_t moe_layer_host_pipeline_workspace_size(const moe_layer_weights* w, int64_t T);
+moe_status moe_layer_forward_host_pipelined(const moe_layer_weights* w, const uint16_t* u_host, int64_t T,
+                                            uint16_t* out_host, const moe_layer_outputs* outs, int update_bias,
+                                            int slot, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                            void* done_event);
+
 #ifdef __cplusplus
 }
 #endif

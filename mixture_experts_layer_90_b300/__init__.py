@@ -30,6 +30,7 @@ EXPORTS = [
     "moe_combine", "moe_bias_update",
     "moe_layer_workspace_size", "moe_layer_forward",
     "moe_layer_host_workspace_size", "moe_layer_forward_host",
+    "moe_layer_host_pipeline_workspace_size", "moe_layer_forward_host_pipelined",
 ]
 
 
@@ -92,6 +93,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_host_workspace_size": (sz, [ctypes.POINTER(LayerWeights), i64]),
         "moe_layer_forward_host": (i32, [ctypes.POINTER(LayerWeights), vp, i64, vp,
                                          ctypes.POINTER(LayerOutputs), i32, vp, sz, vp]),
+        "moe_layer_host_pipeline_workspace_size": (sz, [ctypes.POINTER(LayerWeights), i64]),
+        "moe_layer_forward_host_pipelined": (i32, [ctypes.POINTER(LayerWeights), vp, i64, vp,
+                                                   ctypes.POINTER(LayerOutputs), i32, i32, vp, sz, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

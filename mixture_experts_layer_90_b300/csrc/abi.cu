@@ -2,6 +2,7 @@
 // launch sequence of the layer. No entry point allocates device memory.
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 #include "gemm.cuh"
@@ -269,7 +270,9 @@ struct LayerWs {
         out_dev, total;
 };
 
-LayerWs layer_ws(const moe_layer_weights* w, int64_t T, bool host) {
+// host_slots: device copies of u and h' kept in the workspace (0: none; 1: the
+// host-buffer call; 2: the pipelined host-buffer call, slots alternating)
+LayerWs layer_ws(const moe_layer_weights* w, int64_t T, int host_slots) {
     LayerWs L{};
     const int64_t R = T * w->K + T;
     size_t o = 0;
@@ -291,8 +294,8 @@ LayerWs layer_ws(const moe_layer_weights* w, int64_t T, bool host) {
     L.act = take(size_t(R) * w->I * es);
     L.act_scales = take(w->fp8 ? size_t(w->I / 128) * R * 4 : 0);
     L.y = take(size_t(R) * w->d * 2);
-    L.u_dev = take(host ? size_t(T) * w->d * 2 : 0);
-    L.out_dev = take(host ? size_t(T) * w->d * 2 : 0);
+    L.u_dev = take(size_t(host_slots) * size_t(T) * w->d * 2);
+    L.out_dev = take(size_t(host_slots) * size_t(T) * w->d * 2);
     L.total = o;
     return L;
 }
@@ -309,9 +312,9 @@ moe_status check_layer(const moe_layer_weights* w) {
 
 }  // namespace
 
-size_t moe_layer_workspace_size(const moe_layer_weights* w, int64_t T) { return w ? layer_ws(w, T, false).total : 0; }
+size_t moe_layer_workspace_size(const moe_layer_weights* w, int64_t T) { return w ? layer_ws(w, T, 0).total : 0; }
 size_t moe_layer_host_workspace_size(const moe_layer_weights* w, int64_t T) {
-    return w ? layer_ws(w, T, true).total : 0;
+    return w ? layer_ws(w, T, 1).total : 0;
 }
 
 static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
@@ -377,7 +380,7 @@ moe_status moe_layer_forward(const moe_layer_weights* w, const uint16_t* u, int6
     STATUS_OK(check_layer(w));
     REQUIRE(outs && outs->loads, "moe_layer_forward: outputs need a loads buffer");
     REQUIRE(T >= 0 && (T == 0 || (u && out)), "moe_layer_forward: null u/out");
-    const LayerWs L = layer_ws(w, T, false);
+    const LayerWs L = layer_ws(w, T, 0);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MOE_ERR_WORKSPACE, "moe_layer_forward: workspace needs %zu bytes, 256-byte aligned", L.total);
     return layer_forward(w, u, T, out, outs, update_bias, reinterpret_cast<uint8_t*>(workspace), L, stream);
@@ -389,7 +392,7 @@ moe_status moe_layer_forward_host(const moe_layer_weights* w, const uint16_t* u_
     STATUS_OK(check_layer(w));
     REQUIRE(outs && outs->loads, "moe_layer_forward_host: outputs need a loads buffer");
     REQUIRE(T >= 0 && (T == 0 || (u_host && out_host)), "moe_layer_forward_host: null u/out");
-    const LayerWs L = layer_ws(w, T, true);
+    const LayerWs L = layer_ws(w, T, 1);
     if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MOE_ERR_WORKSPACE, "moe_layer_forward_host: workspace needs %zu bytes", L.total);
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
@@ -399,6 +402,90 @@ moe_status moe_layer_forward_host(const moe_layer_weights* w, const uint16_t* u_
     CUDA_OK(cudaMemcpyAsync(u_dev, u_host, bytes, cudaMemcpyHostToDevice, stream));
     STATUS_OK(layer_forward(w, u_dev, T, out_dev, outs, update_bias, ws, L, stream));
     CUDA_OK(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, stream));
+    return MOE_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Pipelined host-buffer layer: consecutive calls overlap their copies with
+// each other's compute (two device slots for u and h', two copy streams).
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct HostPipeline {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t h2d_done[2] = {}, compute_done[2] = {}, d2h_done[2] = {};
+    bool ready = false;
+};
+constexpr int kMaxPipeDevices = 64;
+std::mutex g_pipe_mutex;
+HostPipeline g_pipe[kMaxPipeDevices];
+
+// The current device's copy streams and events, created on first use and kept
+// for the life of the process.
+moe_status host_pipeline(HostPipeline** out) {
+    int dev = 0;
+    CUDA_OK(cudaGetDevice(&dev));
+    REQUIRE(dev >= 0 && dev < kMaxPipeDevices, "pipelined host call: device %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipeline& p = g_pipe[dev];
+    if (!p.ready) {
+        CUDA_OK(cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking));
+        CUDA_OK(cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking));
+        for (int i = 0; i < 2; ++i) {
+            CUDA_OK(cudaEventCreateWithFlags(&p.h2d_done[i], cudaEventDisableTiming));
+            CUDA_OK(cudaEventCreateWithFlags(&p.compute_done[i], cudaEventDisableTiming));
+            CUDA_OK(cudaEventCreateWithFlags(&p.d2h_done[i], cudaEventDisableTiming));
+        }
+        p.ready = true;
+    }
+    *out = &p;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_layer_host_pipeline_workspace_size(const moe_layer_weights* w, int64_t T) {
+    return w ? layer_ws(w, T, 2).total : 0;
+}
+
+moe_status moe_layer_forward_host_pipelined(const moe_layer_weights* w, const uint16_t* u_host, int64_t T,
+                                            uint16_t* out_host, const moe_layer_outputs* outs, int update_bias,
+                                            int slot, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                            void* done_event) {
+    STATUS_OK(check_layer(w));
+    REQUIRE(outs && outs->loads, "moe_layer_forward_host_pipelined: outputs need a loads buffer");
+    REQUIRE(T >= 0 && (T == 0 || (u_host && out_host)), "moe_layer_forward_host_pipelined: null u/out");
+    REQUIRE(slot == 0 || slot == 1, "moe_layer_forward_host_pipelined: slot must be 0 or 1");
+    REQUIRE(done_event, "moe_layer_forward_host_pipelined: null done event");
+    const LayerWs L = layer_ws(w, T, 2);
+    if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_layer_forward_host_pipelined: workspace needs %zu bytes", L.total);
+    HostPipeline* P = nullptr;
+    STATUS_OK(host_pipeline(&P));
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    const size_t bytes = size_t(T) * w->d * 2;
+    uint16_t* u_dev = reinterpret_cast<uint16_t*>(ws + L.u_dev + slot * bytes);
+    uint16_t* out_dev = reinterpret_cast<uint16_t*>(ws + L.out_dev + slot * bytes);
+    cudaEvent_t done = reinterpret_cast<cudaEvent_t>(done_event);
+    // 1. copy u in once the compute that last read this slot has finished
+    CUDA_OK(cudaStreamWaitEvent(P->h2d, P->compute_done[slot], 0));
+    if (bytes) CUDA_OK(cudaMemcpyAsync(u_dev, u_host, bytes, cudaMemcpyHostToDevice, P->h2d));
+    CUDA_OK(cudaEventRecord(P->h2d_done[slot], P->h2d));
+    // 2. compute on the caller's stream once u is in and this slot's last h' has been copied out
+    CUDA_OK(cudaStreamWaitEvent(stream, P->h2d_done[slot], 0));
+    CUDA_OK(cudaStreamWaitEvent(stream, P->d2h_done[slot], 0));
+    STATUS_OK(layer_forward(w, u_dev, T, out_dev, outs, update_bias, ws, L, stream));
+    CUDA_OK(cudaEventRecord(P->compute_done[slot], stream));
+    // 3. copy h' out; `done` completes when out_host holds it
+    CUDA_OK(cudaStreamWaitEvent(P->d2h, P->compute_done[slot], 0));
+    if (bytes) CUDA_OK(cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, P->d2h));
+    CUDA_OK(cudaEventRecord(P->d2h_done[slot], P->d2h));
+    CUDA_OK(cudaEventRecord(done, P->d2h));
     return MOE_OK;
 }
 

@@ -72,12 +72,14 @@ class MoELayer:
                 w2[e].copy_(w2e)
         return cls(d, N, K, I, centroids, bias, w13, w2, s13, s2, **kw)
 
-    def workspace(self, T: int, host: bool = False) -> torch.Tensor:
+    def workspace(self, T: int, host=False) -> torch.Tensor:
+        """host: False (device buffers), True (host-buffer call) or "pipeline"."""
         key = (T, host)
         ws = self._ws.get(key)
         if ws is None:
             L = load_library()
-            f = L.moe_layer_host_workspace_size if host else L.moe_layer_workspace_size
+            f = (L.moe_layer_host_pipeline_workspace_size if host == "pipeline" else
+                 L.moe_layer_host_workspace_size if host else L.moe_layer_workspace_size)
             need = f(ctypes.byref(self._desc), T)
             ws = torch.empty((max(int(need), 1),), dtype=torch.uint8, device=self.centroids.device)
             self._ws[key] = ws
@@ -118,4 +120,19 @@ class MoELayer:
                                                      ctypes.c_void_p(out_host.data_ptr()), ctypes.byref(outs),
                                                      int(update_bias), _p(ws), ws.numel(), _stream()),
                "moe_layer_forward_host")
+        return out_host
+
+    def forward_host_pipelined(self, u_host: torch.Tensor, out_host: torch.Tensor, slot: int,
+                               done: torch.cuda.Event, update_bias: bool = True):
+        """Pipelined host-buffer forward: alternate slot 0/1 between consecutive
+        calls; `done` (an Event) completes once out_host holds h'."""
+        T = u_host.shape[0]
+        ws = self.workspace(T, host="pipeline")
+        outs = self._outs(None, None)
+        if done.cuda_event == 0:        # torch creates the CUDA event on its first record
+            done.record()
+        _check(load_library().moe_layer_forward_host_pipelined(
+            ctypes.byref(self._desc), ctypes.c_void_p(u_host.data_ptr()), T, ctypes.c_void_p(out_host.data_ptr()),
+            ctypes.byref(outs), int(update_bias), int(slot), _p(ws), ws.numel(), _stream(),
+            ctypes.c_void_p(done.cuda_event)), "moe_layer_forward_host_pipelined")
         return out_host

@@ -115,3 +115,21 @@ def test_layer_host_buffers_match_device_path():
     layer.forward_host(u_h, out_h, update_bias=False)
     torch.cuda.synchronize()
     assert torch.equal(out_h.view(torch.int16), out_d.view(torch.int16))
+
+
+def test_layer_pipelined_host_calls_match_device_path():
+    """Four consecutive pipelined host-buffer calls (slots 0,1,0,1, different
+    batches) give exactly what the device-buffer call gives for each batch."""
+    sh = S.LayerShape(T=160, d=512, N=32, K=4, I=256, name="pipe")
+    layer = _build(sh)
+    us = [S.tokens(sh, seed=10 + i) for i in range(4)]
+    expect = [layer.forward(u.cuda(), update_bias=False).cpu() for u in us]
+    u_h = [u.pin_memory() for u in us]
+    out_h = [torch.empty_like(u).pin_memory() for u in us]
+    done = [torch.cuda.Event() for _ in us]
+    for i in range(4):
+        layer.forward_host_pipelined(u_h[i], out_h[i], slot=i % 2, done=done[i], update_bias=False)
+    for i in range(4):
+        done[i].synchronize()
+        assert torch.equal(out_h[i].view(torch.int16), expect[i].view(torch.int16)), i
+    assert _lib().device_status() == 0
