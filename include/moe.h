@@ -212,6 +212,14 @@ moe_status moe_combine(const uint16_t* u, const uint16_t* y_shared, const uint16
 moe_status moe_bias_update(float* bias, const int32_t* loads, int N, int64_t T, int K, float gamma,
                            moe_stream_t stream);
 
+/* Self-test of the device-side failure detection; the paper has no
+ * counterpart. Launches one thread that waits, with the pipelines' bounded
+ * wait and a limit of limit_ns (at most 1 s), on an mbarrier that nothing
+ * arrives on. It gives up, records MOE_ERR_TIMEOUT in the device status word
+ * (read it with moe_get_device_status) and returns; the CUDA context stays
+ * usable. */
+moe_status moe_selftest_wait_timeout(int64_t limit_ns, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* The whole layer, composed from the calls above.                           */
 /* ------------------------------------------------------------------------ */

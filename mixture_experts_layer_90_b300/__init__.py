@@ -27,7 +27,7 @@ EXPORTS = [
     "moe_route_workspace_size", "moe_route",
     "moe_permute_workspace_size", "moe_permute", "moe_permute_static",
     "fp8_grouped_gemm", "bf16_grouped_gemm",
-    "moe_combine", "moe_bias_update",
+    "moe_combine", "moe_bias_update", "moe_selftest_wait_timeout",
     "moe_layer_workspace_size", "moe_layer_forward",
     "moe_layer_host_workspace_size", "moe_layer_forward_host",
     "moe_layer_host_pipeline_workspace_size", "moe_layer_forward_host_pipelined",
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "bf16_grouped_gemm": (i32, [vp, vp, vp, i32, i64, i32, i32, i32, vp, vp]),
         "moe_combine": (i32, [vp, vp, vp, vp, vp, i64, i32, i32, i64, vp, vp]),
         "moe_bias_update": (i32, [vp, vp, i32, i64, i32, flt, vp]),
+        "moe_selftest_wait_timeout": (i32, [i64, vp]),
         "moe_layer_workspace_size": (sz, [ctypes.POINTER(LayerWeights), i64]),
         "moe_layer_forward": (i32, [ctypes.POINTER(LayerWeights), vp, i64, vp, ctypes.POINTER(LayerOutputs),
                                     i32, vp, sz, vp]),
@@ -266,6 +267,12 @@ def moe_combine(u, y_shared, y_perm, gates, dest_row, out=None):
     _check(load_library().moe_combine(_p(u), _p(y_shared), _p(y_perm), _p(gates), _p(dest_row), T, d, K,
                                       y_perm.shape[0], _p(out), _stream()), "moe_combine")
     return out
+
+
+def moe_selftest_wait_timeout(limit_ns: int):
+    """Launches a bounded wait that must time out (see include/moe.h)."""
+    _require_cuda()
+    _check(load_library().moe_selftest_wait_timeout(int(limit_ns), _stream()), "moe_selftest_wait_timeout")
 
 
 def moe_bias_update(bias, loads, T, K, gamma):

@@ -251,6 +251,13 @@ moe_status moe_combine(const uint16_t* u, const uint16_t* y_shared, const uint16
     return MOE_OK;
 }
 
+moe_status moe_selftest_wait_timeout(int64_t limit_ns, moe_stream_t stream) {
+    REQUIRE(limit_ns > 0 && limit_ns <= 1000000000, "moe_selftest_wait_timeout: limit %lld ns not in (0, 1 s]",
+            (long long)limit_ns);
+    CUDA_OK(moe::launch_wait_timeout_selftest(uint64_t(limit_ns), stream));
+    return MOE_OK;
+}
+
 moe_status moe_bias_update(float* bias, const int32_t* loads, int N, int64_t T, int K, float gamma,
                            moe_stream_t stream) {
     REQUIRE(N >= 1 && T >= 0 && K >= 1, "moe_bias_update: bad sizes");

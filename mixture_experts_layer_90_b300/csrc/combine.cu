@@ -72,7 +72,25 @@ __global__ void bias_update_kernel(float* __restrict__ bias, const int32_t* __re
     else if (lhs < mean_num) bias[i] = __fadd_rn(bias[i], gamma);
 }
 
+// One thread waits on an mbarrier that nothing arrives on, with the same
+// bounded wait as the pipelines (a limit of `limit_ns`): it must give up,
+// record MOE_ERR_TIMEOUT in the status word and return.
+__global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    mbar_wait_for(smem_u32(&bar), 0, &abort_flag, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const uint16_t* u, const uint16_t* y_shared, const uint16_t* y_perm, const float* gates,
                            const int32_t* dest_row, int64_t T, int d, int K, int64_t R, uint16_t* out,

@@ -59,20 +59,23 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Waits for the phase of parity `parity` to complete. Returns false (and
-// records MOE_ERR_TIMEOUT) if it did not within kWaitLimitNs, or at once if
-// *abort is set by another role of the block.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// records MOE_ERR_TIMEOUT, and sets *abort for the other roles of the block)
+// if it did not within limit_ns, or at once if *abort is already set.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_test(bar, parity)) return true;
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             report(MOE_ERR_TIMEOUT);
             *abort = 1;
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    return mbar_wait_for(bar, parity, abort, kWaitLimitNs);
 }
 // Bounded wait with an explicit limit and no abort flag (used while draining).
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, uint64_t limit_ns) {

@@ -36,6 +36,7 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
 cudaError_t launch_combine(const uint16_t* u, const uint16_t* y_shared, const uint16_t* y_perm, const float* gates,
                            const int32_t* dest_row, int64_t T, int d, int K, int64_t R, uint16_t* out,
                            cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_bias_update(float* bias, const int32_t* loads, int N, int64_t T, int K, float gamma,
                                cudaStream_t stream);
 

@@ -119,7 +119,11 @@ __global__ void __launch_bounds__(256) perm_rank_kernel(const int32_t* __restric
             const int64_t p = pb + lane;
             const bool active = p < p1;
             int e = active ? __ldg(idx + p) : -1 - lane;
-            if (e >= N) e = -1 - lane;   // out of range: reported by the count pass
+            if (e < 0 || e >= N) {
+                // out of range (reported by the count pass): the pair gets no row
+                if (active) dest_row[p] = -1;
+                e = -1 - lane;
+            }
             const uint32_t peers = __match_any_sync(0xffffffffu, e);
             if (active && e >= 0) {
                 const int before = __popc(peers & ((1u << lane) - 1u));
@@ -156,7 +160,9 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint16_t* __res
             if constexpr (!kFP8) {
                 for (int k = 0; k < n_dest; ++k) {
                     const int row = __shfl_sync(0xffffffffu, my_dest, k);
-                    if (active) *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + int64_t(row) * d + col) = v;
+                    // rows outside [0, R) come from out-of-range expert ids: skipped
+                    if (active && row >= 0 && row < R)
+                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + int64_t(row) * d + col) = v;
                 }
             } else {
                 float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint16_t* __res
                 const int kb = col / 128;
                 for (int k = 0; k < n_dest; ++k) {
                     const int row = __shfl_sync(0xffffffffu, my_dest, k);
-                    if (active) {
+                    if (active && row >= 0 && row < R) {
                         *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(out) + int64_t(row) * d + col) =
                             make_uint2(w0, w1);
                         if (l == 0) scales[int64_t(kb) * R + row] = sc;
