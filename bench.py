@@ -124,6 +124,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks (the slowest rank's time); x itself when
+    torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
@@ -258,11 +270,7 @@ def run_ours(args):
         barrier()
     status = moe.device_status()
     assert status == 0, f"device status {status}"
-    elapsed_ms = t0.elapsed_time(t1)
-    if ws > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dev)
     stage_ms = {name: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in events)
                 for j, name in enumerate(moe.LAYER_STAGES)}
 
@@ -284,11 +292,7 @@ def run_ours(args):
         layer.forward_host_pipelined(u_host[i % 2], out_host[i % 2], slot=i % 2, done=done[i])
     done[e_steps - 1].synchronize()
     barrier()
-    e2e_ms = 1000.0 * (time.perf_counter() - w0)
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(1000.0 * (time.perf_counter() - w0), dev)
     assert moe.device_status() == 0
 
     tokens = sh.T * args.steps * ws

@@ -6,11 +6,12 @@ leg may import this package. It wraps the plain C file `moe_oracle.c`
 composes its pieces into the layer. It shares no code with the CUDA library
 and never imports it.
 
-Parity pins: every function here is checked in tests/test_oracle_*.py
-against something other than itself (closed forms, brute force with numpy,
-torch's float8_e4m3fn conversion, invariants). The layer value at the full
-V3 shape has no printed worked example to compare with; it is pinned only
-through its stages.
+Parity pins: every function here is checked in tests/test_oracle_*.py and
+tests/test_golden_pages.py against something other than itself (closed forms,
+brute force with numpy, torch's float8_e4m3fn conversion, invariants, the
+figures the pages print). The composed layer is checked against an
+independent brute force on a tiny layer; the pages print no worked example at
+the full V3 shape, so the full-size value rests on those pins.
 """
 from __future__ import annotations
 

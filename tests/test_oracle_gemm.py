@@ -181,3 +181,83 @@ def test_limited_accumulation_diagnostic():
     err32 = np.max(np.abs(acc32 - exact) / np.abs(exact))
     assert 2e-3 < err14 < 0.2
     assert err32 < 1e-5
+
+
+def _bruteforce_layer(u, cent, bias, K, weights):
+    """The layer formula (nlp-lineage page, "The notation") on tiny inputs,
+    written independently of the oracle: numpy FP64 routing, torch's
+    float8_e4m3fn conversion for every 1x128 / 128x128 quantisation, FP64
+    matmuls, bf16 rounding of each expert output by torch."""
+    uf = u.double().numpy()
+    z = uf @ cent.double().numpy().T
+    s = 1.0 / (1.0 + np.exp(-z))
+    key = s + bias.double().numpy()[None, :]
+    T, d = uf.shape
+
+    def q1x128(x32):                       # rows of fp32 values
+        x = torch.as_tensor(x32, dtype=torch.float32).reshape(x32.shape[0], -1, 128)
+        amax = x.abs().amax(-1, keepdim=True)
+        sc = torch.where(amax == 0, torch.ones_like(amax), amax / 448.0)
+        q = (x / sc).to(torch.float8_e4m3fn).to(torch.float64)
+        return (q * sc.double()).reshape(x32.shape[0], -1).numpy()
+
+    def q128x128(w):
+        x = w.float()
+        r, c = x.shape
+        xb = x.reshape(r // 128, 128, c // 128, 128)
+        amax = xb.abs().amax(dim=(1, 3), keepdim=True)
+        sc = torch.where(amax == 0, torch.ones_like(amax), amax / 448.0)
+        q = (xb / sc).to(torch.float8_e4m3fn).to(torch.float64)
+        return (q * sc.double()).reshape(r, c).numpy()
+
+    def ffn(xdq, e):
+        w1, w3, w2 = weights(e)
+        h1, h3 = xdq @ q128x128(w1).T, xdq @ q128x128(w3).T
+        a = h1 / (1 + np.exp(-h1)) * h3
+        y = q1x128(a.astype(np.float32)) @ q128x128(w2).T
+        return torch.as_tensor(y).to(torch.float32).to(torch.bfloat16).double().numpy()
+
+    X = q1x128(u.float().numpy())
+    out = uf + ffn(X, cent.shape[0])
+    for t in range(T):
+        chosen = np.sort(np.argsort(-key[t], kind="stable")[:K])
+        g = s[t, chosen] / s[t, chosen].sum()
+        for k, e in enumerate(chosen):
+            out[t] += g[k] * ffn(X[t:t + 1], e)[0]
+    return out
+
+
+def test_layer_composition_matches_independent_bruteforce():
+    """oracle.layer_tokens (routing, 1x128 / 128x128 quantisation, SwiGLU FFNs,
+    re-quantised intermediate, bf16 expert outputs, shared expert, gate-weighted
+    sum) against the brute force above; the bias range is wide so that a bias
+    leaking into the gate, a dropped shared expert or a swapped gate/up
+    projection all show up far above the rounding differences."""
+    sh = S.LayerShape(T=6, d=256, N=8, K=3, I=128, name="bf")
+    u = S.tokens(sh)
+    cent = S.centroids(sh)
+    bias = S.uniform((sh.N,), -0.5, 0.5, S.key(7, "bf-bias"))
+    wts = {e: S.expert_weights(sh, e) for e in range(sh.N + 1)}
+    got, r, _ = oracle.layer_tokens(u, cent, bias, sh.K, lambda e: wts[e], np.arange(sh.T), fp8=True)
+    ref = _bruteforce_layer(u, cent, bias, sh.K, lambda e: wts[e])
+    scale = np.abs(ref - u.double().numpy()).max()
+    # Both sides compute the same roundings; they may differ only in FP64 summation
+    # order (~1e-16) or, were an expert output to land on a bf16 rounding boundary,
+    # by the brute force's fp32 step there (none does for these seeded inputs).
+    # A bias leaking into the gates moves them by ~0.18 here.
+    assert np.max(np.abs(got - ref)) <= 1e-9 * scale, np.max(np.abs(got - ref)) / scale
+
+
+def test_layer_with_zero_down_projections_returns_u():
+    """W2 = 0 for every expert (routed and shared): h' equals u exactly."""
+    sh = S.LayerShape(T=5, d=256, N=8, K=2, I=128, name="w2zero")
+    u = S.tokens(sh)
+    cent = S.centroids(sh)
+    bias = S.bias(sh)
+
+    def wts(e):
+        w1, w3, w2 = S.expert_weights(sh, e)
+        return w1, w3, torch.zeros_like(w2)
+    for fp8 in (True, False):
+        got, _, _ = oracle.layer_tokens(u, cent, bias, sh.K, wts, np.arange(sh.T), fp8=fp8)
+        np.testing.assert_array_equal(got, u.double().numpy())
