@@ -152,11 +152,14 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint16_t* __res
         if (lane < K) my_dest = __ldg(dest_row + t * K + lane);
         else if (lane == K && with_shared) my_dest = int(int64_t(T) * K + t);
         const uint16_t* src = x + t * d;
+        // the next 256-column chunk is loaded while this one is written (two loads in flight)
+        uint4 v_next = make_uint4(0, 0, 0, 0);
+        if (half * 128 + l * 8 < d) v_next = __ldg(reinterpret_cast<const uint4*>(src + half * 128 + l * 8));
         for (int c0 = 0; c0 < d; c0 += 256) {
             const int col = c0 + half * 128 + l * 8;     // 8 elements per lane
             const bool active = col < d;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (active) v = __ldg(reinterpret_cast<const uint4*>(src + col));
+            const uint4 v = v_next;
+            if (col + 256 < d) v_next = __ldg(reinterpret_cast<const uint4*>(src + col + 256));
             if constexpr (!kFP8) {
                 for (int k = 0; k < n_dest; ++k) {
                     const int row = __shfl_sync(0xffffffffu, my_dest, k);
