@@ -280,7 +280,9 @@ moe_status moe_layer_forward_host(const moe_layer_weights* w, const uint16_t* u_
  * out_host; a synchronisation of `stream` alone does NOT cover that copy.
  * out_host may be read, and u_host overwritten, once `done_event` has
  * completed. The copy streams and events are created on the first call on a
- * device and live until the process exits. */
+ * device and live until the process exits. They are shared by every
+ * pipelined call on that device: calls from different workspaces stay
+ * correct but wait on one another's copies of the same slot index. */
 size_t moe_layer_host_pipeline_workspace_size(const moe_layer_weights* w, int64_t T);
 moe_status moe_layer_forward_host_pipelined(const moe_layer_weights* w, const uint16_t* u_host, int64_t T,
                                             uint16_t* out_host, const moe_layer_outputs* outs, int update_bias,
