@@ -192,7 +192,7 @@ moe_status fp8_grouped_gemm(const uint8_t* A, const float* sa, const uint8_t* B,
     a.Nd = Nd;
     a.Kd = Kd;
     a.k_steps = Kd / 128;
-    a.a_k_steps = Kd / 128;
+    a.a_k_repeat = 1;
     a.elems_per_step = 128;
     a.splits = 1;
     a.epilogue = epilogue;
@@ -230,7 +230,7 @@ moe_status bf16_grouped_gemm(const uint16_t* A, const uint16_t* B, const int32_t
     a.Nd = Nd;
     a.Kd = Kd;
     a.k_steps = Kd / 64;
-    a.a_k_steps = Kd / 64;
+    a.a_k_repeat = 1;
     a.elems_per_step = 64;
     a.splits = 1;
     a.promote_steps = moe::kBf16PromoteSteps;

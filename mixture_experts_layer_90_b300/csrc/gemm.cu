@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b_row = it.g * args.Nd + it.nt * kBN;
                 const int k0 = it.sp * steps_per_split;
                 const int k1 = min(args.k_steps, k0 + steps_per_split);
-                int ka = k0 % args.a_k_steps;   // A's K step (A wraps around for the split routing gate)
+                int ka = k0 / args.a_k_repeat;   // A's K step
+                int rep = k0 - ka * args.a_k_repeat;
                 for (int ks = k0; ks < k1; ++ks) {
                     if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort)) {
                         stop = true;
@@ -199,7 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(ringA + stage * kABytes, &tmA, fb, ka * args.elems_per_step, a_row);
                     tma_load_2d(ringB + stage * kBBytes, &tmB, fb, ks * args.elems_per_step, b_row);
                     armed[stage] += 1;
-                    if (++ka == args.a_k_steps) ka = 0;
+                    if (++rep == args.a_k_repeat) {
+                        rep = 0;
+                        ++ka;
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;

@@ -21,7 +21,8 @@ struct GemmArgs {
     int Nd;              // output columns per group, multiple of 256
     int Kd;              // K extent of B in elements (FP8: also of A)
     int k_steps;         // 128-byte K steps per output tile (before split)
-    int a_k_steps;       // A's K extent in steps; A's step = step % a_k_steps
+    int a_k_repeat;      // B steps per A step: A's step = step / a_k_repeat (1 for a plain GEMM;
+                         // the routing gate's B interleaves its split terms per 64-column block)
     int elems_per_step;  // 128 (e4m3) or 64 (bf16)
     int splits;          // split-K parts (MOE_EPI_F32 only; else 1)
     int promote_steps;   // bf16: K steps accumulated in TMEM before adding into fp32 registers

@@ -138,55 +138,69 @@ __global__ void __launch_bounds__(256) perm_rank_kernel(const int32_t* __restric
     }
 }
 
-// Token-major scatter of rows (bf16 copy or E4M3 1x128 quantisation).
+// Token-major scatter of rows (bf16 copy or E4M3 1x128 quantisation). A warp
+// owns one token and moves 512 columns per step, 16 per lane:
+//   E4M3: lane l takes columns 16l..16l+15, so a 128-element tile sits in 8
+//         lanes and each destination row gets one 16-byte store per lane
+//         (512 contiguous bytes per warp);
+//   bf16: lane l takes columns 8l..8l+7 and 256+8l..256+8l+7, so each of
+//         the two 16-byte stores per destination covers 512 contiguous bytes.
+// The next step's columns are loaded while this step's are written.
 template <bool kFP8>
 __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint16_t* __restrict__ x, int64_t T, int d, int K,
                                                            const int32_t* __restrict__ dest_row, int with_shared,
                                                            void* __restrict__ out, float* __restrict__ scales,
                                                            int64_t R) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int half = lane >> 4, l = lane & 15;
     const int n_dest = K + (with_shared ? 1 : 0);
+    const int off_a = kFP8 ? lane * 16 : lane * 8;    // columns of the lane's two 8-element pieces
+    const int off_b = kFP8 ? lane * 16 + 8 : 256 + lane * 8;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
     for (int64_t t = int64_t(blockIdx.x) * 8 + w; t < T; t += int64_t(gridDim.x) * 8) {
         int my_dest = 0;
         if (lane < K) my_dest = __ldg(dest_row + t * K + lane);
         else if (lane == K && with_shared) my_dest = int(int64_t(T) * K + t);
         const uint16_t* src = x + t * d;
-        // the next 256-column chunk is loaded while this one is written (two loads in flight)
-        uint4 v_next = make_uint4(0, 0, 0, 0);
-        if (half * 128 + l * 8 < d) v_next = __ldg(reinterpret_cast<const uint4*>(src + half * 128 + l * 8));
-        for (int c0 = 0; c0 < d; c0 += 256) {
-            const int col = c0 + half * 128 + l * 8;     // 8 elements per lane
-            const bool active = col < d;
-            const uint4 v = v_next;
-            if (col + 256 < d) v_next = __ldg(reinterpret_cast<const uint4*>(src + col + 256));
+        uint4 n0 = off_a < d ? __ldg(reinterpret_cast<const uint4*>(src + off_a)) : zero;
+        uint4 n1 = off_b < d ? __ldg(reinterpret_cast<const uint4*>(src + off_b)) : zero;
+        for (int c0 = 0; c0 < d; c0 += 512) {
+            const int ca = c0 + off_a, cb = c0 + off_b;
+            // d is a multiple of 128: the 8 lanes of an E4M3 tile are all active or all idle
+            const bool act_a = ca < d, act_b = cb < d;
+            const uint4 v0 = n0, v1 = n1;
+            if (ca + 512 < d) n0 = __ldg(reinterpret_cast<const uint4*>(src + ca + 512));
+            if (cb + 512 < d) n1 = __ldg(reinterpret_cast<const uint4*>(src + cb + 512));
             if constexpr (!kFP8) {
                 for (int k = 0; k < n_dest; ++k) {
                     const int row = __shfl_sync(0xffffffffu, my_dest, k);
                     // rows outside [0, R) come from out-of-range expert ids: skipped
-                    if (active && row >= 0 && row < R)
-                        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + int64_t(row) * d + col) = v;
+                    if (row >= 0 && row < R) {
+                        uint16_t* dst = reinterpret_cast<uint16_t*>(out) + int64_t(row) * d;
+                        if (act_a) *reinterpret_cast<uint4*>(dst + ca) = v0;
+                        if (act_b) *reinterpret_cast<uint4*>(dst + cb) = v1;
+                    }
                 }
             } else {
-                float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                              bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+                const uint32_t in[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
                 float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(in[i])), fabsf(bf16_hi(in[i]))));
 #pragma unroll
-                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
                 const float sc = tile_scale(amax);
-                const uint32_t w0 = pack_e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
-                                    (pack_e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
-                const uint32_t w1 = pack_e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
-                                    (pack_e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
-                const int kb = col / 128;
+                uint32_t q[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    q[i] = pack_e4m3x2(__fdiv_rn(bf16_lo(in[2 * i]), sc), __fdiv_rn(bf16_hi(in[2 * i]), sc)) |
+                           (pack_e4m3x2(__fdiv_rn(bf16_lo(in[2 * i + 1]), sc), __fdiv_rn(bf16_hi(in[2 * i + 1]), sc))
+                            << 16);
+                const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+                const int kb = ca / 128;
                 for (int k = 0; k < n_dest; ++k) {
                     const int row = __shfl_sync(0xffffffffu, my_dest, k);
-                    if (active && row >= 0 && row < R) {
-                        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(out) + int64_t(row) * d + col) =
-                            make_uint2(w0, w1);
-                        if (l == 0) scales[int64_t(kb) * R + row] = sc;
+                    if (act_a && row >= 0 && row < R) {
+                        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + int64_t(row) * d + ca) = qv;
+                        if ((lane & 7) == 0) scales[int64_t(kb) * R + row] = sc;
                     }
                 }
             }

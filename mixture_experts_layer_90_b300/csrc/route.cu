@@ -11,6 +11,9 @@
 // fp32 centroids are split exactly into three bf16 terms (hi + mid + lo = e,
 // each product with a bf16 token value exact in fp32), so the gate runs as a
 // bf16 GEMM over K = 3d with fp32 accumulation; bf16 centroids need one term.
+// The split operand keeps the three terms of each 64-column block side by side
+// (hi, mid, lo), so a tile of u is fetched once and feeds three consecutive K
+// steps.
 // The GEMM is split along K over enough blocks to fill the GPU; a warp per
 // token then sums the partial logits in a fixed order and selects.
 #include <cuda_bf16.h>
@@ -44,9 +47,10 @@ __global__ void split_centroids_kernel(const void* __restrict__ cent, int f32, i
         const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
         const float r2 = r1 - __bfloat162float(mid);        // exact, fits 8 bits
         const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
-        row[j] = __bfloat16_as_ushort(hi);
-        row[d + j] = __bfloat16_as_ushort(mid);
-        row[2 * d + j] = __bfloat16_as_ushort(lo);
+        uint16_t* blk = row + int64_t(j / 64) * 3 * 64 + (j % 64);
+        blk[0] = __bfloat16_as_ushort(hi);
+        blk[64] = __bfloat16_as_ushort(mid);
+        blk[128] = __bfloat16_as_ushort(lo);
     }
 }
 
@@ -272,7 +276,7 @@ cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* centro
     a.Nd = plan.n_pad;
     a.Kd = plan.terms * d;
     a.k_steps = plan.terms * d / 64;
-    a.a_k_steps = d / 64;
+    a.a_k_repeat = plan.terms;
     a.elems_per_step = 64;
     a.splits = plan.splits;
     a.promote_steps = kBf16PromoteSteps;
