@@ -84,7 +84,7 @@ __device__ __forceinline__ Item decode(int item, const Smem& s, int G, int n_til
 __device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 // 32 bytes to global memory in one instruction (address 32-byte aligned).
-__device__ __forceinline__ void st_global_32B(void* p, const uint32_t (&w)[8]) {
+__device__ __forceinline__ void st_global_32B(void* p, const uint32_t* w) {   // w[0..7]
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
                  "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                  : "memory");
@@ -320,6 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- epilogue warps ----------------
         const int q = warp & 3;        // TMEM lane quarter = rows 32q..32q+31
         const int wg = warp >> 2;      // column slice
+        // SwiGLU tiles pair columns c and 128 + c (gate and up of one output), so a
+        // warp takes 32wg..32wg+31 and 128+32wg..128+32wg+31; the other epilogues
+        // give a warp the 64 contiguous columns 64wg..64wg+63.
+        constexpr bool kContig = (kEpi == MOE_EPI_BF16 || kEpi == MOE_EPI_F32);
+        const uint32_t slice = kContig ? wg * 64 : wg * 32;
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = tmem_base + (uint32_t(q * 32) << 16);
         uint32_t acc_iter = 0, tile_iter = 0;
@@ -360,20 +365,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t col = lane_addr + buf * kBN + wg * 32;
+                    const uint32_t col = lane_addr + buf * kBN + slice;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        // chunks 0,1: columns 32*wg + 0..31 (first weight block);
-                        // chunks 2,3: 128 + 32*wg + 0..31 (second weight block)
+                        // paired slices: chunks 0,1 in the first weight block, 2,3 in the
+                        // second; contiguous slices lie in block wg / 2
                         uint32_t r[16];
-                        tmem_ld_16(col + (c >> 1) * 128 + (c & 1) * 16, r);
+                        tmem_ld_16(col + (kContig ? c * 16 : (c >> 1) * 128 + (c & 1) * 16), r);
                         tmem_wait_ld(r);
                         if (c == 3) {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
                         }
-                        const float f = c < 2 ? fl : fh;
+                        const float f = kContig ? (wg < 2 ? fl : fh) : (c < 2 ? fl : fh);
                         const float2 f2 = make_float2(f, f);
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
@@ -402,11 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t col = lane_addr + buf * kBN + wg * 32;
+                    const uint32_t col = lane_addr + buf * kBN + slice;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[16];
-                        tmem_ld_16(col + (c >> 1) * 128 + (c & 1) * 16, r);
+                        tmem_ld_16(col + (kContig ? c * 16 : (c >> 1) * 128 + (c & 1) * 16), r);
                         tmem_wait_ld(r);
                         if (c == 3) {
                             tc_fence_before();
@@ -475,31 +480,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         st_global_32B(out + 16 * v, w);
                     }
                 }
+            } else if constexpr (ep == MOE_EPI_BF16) {
+                // A thread holds 128 bytes of its row. Four lanes swap 32-byte pieces
+                // (a 4x4 transpose by two xor-shuffle rounds) so that in store i the lanes
+                // 4a..4a+3 write the whole 128 bytes of row 4a+i: 8 full lines per store.
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+                const bool b0 = lane & 1, b1 = lane & 2;
+#pragma unroll
+                for (int c = 0; c < 4; c += 2)
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const uint32_t v = __shfl_xor_sync(0xffffffffu, b0 ? w[8 * c + r] : w[8 * c + 8 + r], 1);
+                        if (b0) w[8 * c + r] = v;
+                        else w[8 * c + 8 + r] = v;
+                    }
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const uint32_t v = __shfl_xor_sync(0xffffffffu, b1 ? w[8 * c + r] : w[8 * c + 16 + r], 2);
+                        if (b1) w[8 * c + r] = v;
+                        else w[8 * c + 16 + r] = v;
+                    }
+                const int rows = s.offs[it.g + 1] - s.offs[it.g];
+                const int64_t c0 = int64_t(it.nt) * kBN + slice + 16 * (lane & 3);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rl = it.mt * kBM + q * 32 + (lane & ~3) + i;
+                    if (rl < rows)
+                        st_global_32B(reinterpret_cast<uint16_t*>(args.C) + (int64_t(s.offs[it.g]) + rl) * args.Nd + c0,
+                                      w + 8 * i);
+                }
             } else if (valid) {
-                const int64_t c0 = int64_t(it.nt) * kBN + wg * 32;
-                if constexpr (ep == MOE_EPI_BF16) {
-                    uint16_t* out = reinterpret_cast<uint16_t*>(args.C) + grow * args.Nd + c0;
+                // MOE_EPI_F32: split-K partial sums, [splits][M_total][Nd]
+                const int64_t c0 = int64_t(it.nt) * kBN + slice;
+                float* out = reinterpret_cast<float*>(args.C) + (int64_t(it.sp) * args.M_total + grow) * args.Nd + c0;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                for (int v = 0; v < 8; ++v) {
+                    uint32_t w[8];
 #pragma unroll
-                        for (int v = 0; v < 2; ++v) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                w[i] = pack_bf16x2(acc[32 * h + 16 * v + 2 * i], acc[32 * h + 16 * v + 2 * i + 1]);
-                            st_global_32B(out + 128 * h + 16 * v, w);
-                        }
-                } else {  // MOE_EPI_F32: split-K partial sums, [splits][M_total][Nd]
-                    float* out = reinterpret_cast<float*>(args.C) + (int64_t(it.sp) * args.M_total + grow) * args.Nd + c0;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(acc[32 * h + 8 * v + i]);
-                            st_global_32B(out + 128 * h + 8 * v, w);
-                        }
+                    for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(acc[8 * v + i]);
+                    st_global_32B(out + 8 * v, w);
                 }
             }
             tile_iter += 1;

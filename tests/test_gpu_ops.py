@@ -309,7 +309,10 @@ def _rand_topk(T, N, K, seed=0):
 
 
 @pytest.mark.parametrize("T,d,N,K,fp8,shared", [(1, 128, 4, 2, False, False), (1000, 512, 16, 4, False, True),
-                                                 (333, 640, 256, 8, True, True), (64, 256, 1024, 16, True, False)])
+                                                 (333, 640, 256, 8, True, True), (64, 256, 1024, 16, True, False),
+                                                 # widths that leave part of the warp's 512-column step idle
+                                                 (77, 384, 8, 3, False, True), (129, 896, 64, 6, False, False),
+                                                 (50, 128, 4, 2, True, True), (91, 1152, 32, 5, True, False)])
 def test_permute_bit_exact(T, d, N, K, fp8, shared):
     x = bf16((T, d), 1.0, "px", T, d)
     idx = _rand_topk(T, N, K)
