@@ -45,9 +45,12 @@ def profiled_traffic(name):
     if not os.path.exists(p):
         return None
     h = hashlib.sha1()
-    for f in ("gemm.cu", "common.cuh"):
-        with open(os.path.join(ROOT, "mixture_experts_layer_90_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for f in ("gemm.cu", "common.cuh"):   # the code only: // comments and blank lines do not count
+        with open(os.path.join(ROOT, "mixture_experts_layer_90_b300", "csrc", f), encoding="utf-8") as fh:
+            for ln in fh:
+                code = ln.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     for ln in open(p):
         parts = ln.strip().strip("`").split()
         if len(parts) == 3 and parts[0] == name + ":" and parts[2] == h.hexdigest()[:12]:

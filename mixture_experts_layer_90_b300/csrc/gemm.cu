@@ -7,15 +7,17 @@
 //     buffer; epilogue warps read it, multiply by sa[row,kb] * sb[nblk,kb]
 //     and add it into FP32 registers, while the tensor cores fill the other
 //     buffer with the next block.
-//   * bf16 expert GEMMs (FP32 accumulation over the whole K in TMEM).
+//   * bf16 expert GEMMs (TMEM partial sums of 8 K steps added into FP32
+//     registers).
 //   * the gate logits of routing (bf16, split-K partial sums in fp32).
 //
 // Block roles (608 threads):
-//   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and, in
-//               warpgroup w/4, the columns {32*(w/4) + c} and {128 + 32*(w/4) + c};
+//   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows); in
+//               warpgroup w/4 it takes the columns {32*(w/4) + c} and
+//               {128 + 32*(w/4) + c} of a SwiGLU tile (gate and up side by
+//               side), else the 64 contiguous columns {64*(w/4) + c};
 //   warp 16     TMA producer: one lane issues the tile loads and does nothing
-//               else (any other work in its loop delays the loads, and the
-//               tile feed is what bounds this kernel);
+//               else (any other work in its loop delays the loads);
 //   warp 17     tcgen05.mma issuer (one elected lane) + TMEM owner;
 //   warp 18     FP8 scales: each K block's 128 row scales and 2 weight scales
 //               copied into a shared-memory ring (cp.async), so the epilogue
