@@ -117,11 +117,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kSSlots; ++i) {
             mbar_init(smem_u32(&s.sfull[i]), 32);         // one cp.async arrival per producer lane
-            mbar_init(smem_u32(&s.sempty[i]), kEpiWarps);
+            mbar_init(smem_u32(&s.sempty[i]), kEpiWarps * 32);   // every epilogue lane arrives
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s.tfull[i]), 1);
-            mbar_init(smem_u32(&s.tempty[i]), kEpiWarps);
+            mbar_init(smem_u32(&s.tempty[i]), kEpiWarps * 32);
             mbar_init(smem_u32(&s.xchg[i]), kEpiWarps * 32);
         }
         mbar_init(smem_u32(&s.drain), 1);
@@ -355,8 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float sa_v = s.scales[sslot].sa[row_in_tile];
                     const float fl = sa_v * s.scales[sslot].sb[0];
                     const float fh = sa_v * s.scales[sslot].sb[1];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&s.sempty[sslot]));
+                    // each lane releases the slot after its own reads (no warp barrier and
+                    // no single-lane branch in the promotion loop)
+                    mbar_arrive(smem_u32(&s.sempty[sslot]));
                     if (++sslot == kSSlots) {
                         sslot = 0;
                         sphase ^= 1u;
@@ -377,8 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld(r);
                         if (c == 3) {
                             tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+                            mbar_arrive(smem_u32(&s.tempty[buf]));
                         }
                         const float f = kContig ? (wg < 2 ? fl : fh) : (c < 2 ? fl : fh);
                         const float2 f2 = make_float2(f, f);
@@ -417,8 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld(r);
                         if (c == 3) {
                             tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(smem_u32(&s.tempty[buf]));
+                            mbar_arrive(smem_u32(&s.tempty[buf]));
                         }
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
