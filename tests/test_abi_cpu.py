@@ -97,3 +97,58 @@ def test_python_calls_fail_loudly_without_gpu():
         pytest.skip("a GPU is present")
     with pytest.raises(RuntimeError, match="no CUDA device"):
         M.fp8_quant_1x128(torch.zeros((1, 128), dtype=torch.bfloat16))
+
+
+def _v3_weights():
+    p = 4096
+    return M.LayerWeights(d=7168, N=256, K=8, I=2048, n_groups=1, topk_groups=1, gamma=1e-3, fp8=1, centroids=p,
+                          centroid_dtype=1, bias=p, w13=p, w13_scales=p, w2=p, w2_scales=p)
+
+
+def test_pipelined_host_call_checks_its_arguments(L):
+    p, s = _ok_ptr(), ctypes.c_void_p(0)
+    w = _v3_weights()
+    outs = M.LayerOutputs(topk_idx=None, gates=None, loads=4096, stage_events=None)
+    T = 8192
+    need = L.moe_layer_host_pipeline_workspace_size(ctypes.byref(w), T)
+    # two device slots for u and for h' on top of the device-buffer workspace
+    assert need >= L.moe_layer_workspace_size(ctypes.byref(w), T) + 4 * T * 7168 * 2
+    call = lambda slot, ws_bytes, done: L.moe_layer_forward_host_pipelined(  # noqa: E731
+        ctypes.byref(w), p, T, p, ctypes.byref(outs), 1, slot, ctypes.c_void_p(1 << 20), ws_bytes, s, done)
+    assert call(2, need, p) == M.MOE_ERR_INVALID_ARG
+    assert b"slot" in L.moe_last_error()
+    assert call(-1, need, p) == M.MOE_ERR_INVALID_ARG
+    assert call(0, need, None) == M.MOE_ERR_INVALID_ARG
+    assert call(1, need - 1, p) == M.MOE_ERR_WORKSPACE
+    no_loads = M.LayerOutputs(topk_idx=None, gates=None, loads=None, stage_events=None)
+    assert L.moe_layer_forward_host_pipelined(ctypes.byref(w), p, T, p, ctypes.byref(no_loads), 1, 0,
+                                              ctypes.c_void_p(1 << 20), need, s, p) == M.MOE_ERR_INVALID_ARG
+    bad = _v3_weights()
+    bad.d = 7000
+    assert L.moe_layer_forward_host_pipelined(ctypes.byref(bad), p, T, p, ctypes.byref(outs), 1, 0,
+                                              ctypes.c_void_p(1 << 20), need, s, p) == M.MOE_ERR_INVALID_ARG
+
+
+def test_static_permute_checks_its_built_in_scratch_limit(L):
+    p, s = _ok_ptr(), ctypes.c_void_p(0)
+    call = lambda T, d, N, K, dt=M.MOE_DTYPE_BF16: L.moe_permute_static(  # noqa: E731
+        p, T, d, p, N, K, dt, 1, p, p, p, p, p, s)
+    # ceil(T/32)*N + N int32 must fit in 2^20: N = 256 allows T <= 131,040; N = 1024 allows T <= 32,736
+    assert call(131_072, 128, 256, 8) == M.MOE_ERR_WORKSPACE
+    assert b"moe_permute with a workspace" in L.moe_last_error()
+    assert call(40_000, 128, 1024, 8) == M.MOE_ERR_WORKSPACE
+    # the same argument rules as moe_permute
+    assert call(100, 100, 16, 4) == M.MOE_ERR_INVALID_ARG
+    assert call(100, 128, 16, 17) == M.MOE_ERR_INVALID_ARG
+    assert call(100, 128, 2048, 8) == M.MOE_ERR_INVALID_ARG
+    assert call(100, 128, 16, 4, dt=M.MOE_DTYPE_F32) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_permute_static(ctypes.c_void_p(4100), 100, 128, p, 16, 4, M.MOE_DTYPE_BF16, 1, p, p, p, p, p,
+                                s) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_permute_static(p, 100, 128, p, 16, 4, M.MOE_DTYPE_E4M3, 1, p, p, p, p, None,
+                                s) == M.MOE_ERR_INVALID_ARG
+
+
+def test_wait_self_test_limit_is_bounded(L):
+    s = ctypes.c_void_p(0)
+    assert L.moe_selftest_wait_timeout(0, s) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_wait_timeout(2_000_000_000, s) == M.MOE_ERR_INVALID_ARG
