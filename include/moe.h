@@ -66,7 +66,7 @@ enum {
 /* Human-readable text of the last host-side error (thread-local). */
 const char* moe_last_error(void);
 
-/* Number of SMs the kernels size their persistent grids for (device 0 at first call). */
+/* Number of SMs the kernels size their persistent grids for (the current device). */
 int moe_num_sms(void);
 
 /*
@@ -113,6 +113,27 @@ moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids,
                      int32_t* topk_idx, float* gates, int32_t* loads, float* scores,
                      void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/* moe_route in two parts, for centroids that stay fixed across calls (the
+ * centroids are weights of the layer; only the bias changes between steps).
+ * moe_route_prepare_centroids writes the tensor-core operand of the gate once:
+ * fp32 centroids split exactly into three bf16 terms (bf16 centroids are
+ * copied), zero rows up to a multiple of 256 experts. `prepared` is device
+ * memory of moe_route_prepared_centroids_size() bytes, 256-byte aligned,
+ * owned by the caller; it must be prepared again if the centroids change.
+ * moe_route_prepared then routes from it with the same arguments, outputs and
+ * limits as moe_route, and a workspace of moe_route_prepared_workspace_size()
+ * bytes (the split-K partial logits only). The two calls give bit-identical
+ * results to moe_route. */
+size_t moe_route_prepared_centroids_size(int d, int N, int centroid_dtype);
+moe_status moe_route_prepare_centroids(const void* centroids, int centroid_dtype, int N, int d,
+                                       void* prepared, size_t prepared_bytes, moe_stream_t stream);
+size_t moe_route_prepared_workspace_size(int64_t T, int d, int N, int centroid_dtype);
+moe_status moe_route_prepared(const uint16_t* u, int64_t T, int d, const void* prepared,
+                              int centroid_dtype, const float* bias, int N, int K, int n_groups,
+                              int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
+                              float* scores, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Permutation — the single-GPU form of the dispatch step (learn.ifs.name    */
 /* summary, paragraph on all-to-all dispatch/combine): a stable counting     */
@@ -148,7 +169,10 @@ moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_
  *
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress) and caches it. Make that first call
- * before any stream capture.
+ * before any stream capture. The cached address belongs to the CUDA context
+ * of that first call: it is dropped when a launch fails, but it does not
+ * survive cudaDeviceReset, after which this entry point must not be called
+ * again in the same process.
  *
  * Every call on a device shares the one array. The kernels write each
  * scratch entry before reading it, so nothing must start at zero and the
@@ -236,6 +260,8 @@ typedef struct {
     const float* w13_scales;   /* [N+1][2I/128][d/128] (fp8 only)                           */
     const void* w2;            /* [N+1][d][I]                                               */
     const float* w2_scales;    /* [N+1][d/128][I/128] (fp8 only)                            */
+    const void* centroids_prepared; /* NULL, or the output of moe_route_prepare_centroids for
+                                       `centroids` (then the layer routes from it)           */
 } moe_layer_weights;
 
 /* Optional outputs of one forward (any may be NULL except loads). */

@@ -25,6 +25,8 @@ EXPORTS = [
     "moe_last_error", "moe_num_sms", "moe_get_device_status",
     "fp8_quant_1x128", "fp8_quant_128x128",
     "moe_route_workspace_size", "moe_route",
+    "moe_route_prepared_centroids_size", "moe_route_prepare_centroids",
+    "moe_route_prepared_workspace_size", "moe_route_prepared",
     "moe_permute_workspace_size", "moe_permute", "moe_permute_static",
     "fp8_grouped_gemm", "bf16_grouped_gemm",
     "moe_combine", "moe_bias_update", "moe_selftest_wait_timeout",
@@ -47,7 +49,7 @@ class LayerWeights(ctypes.Structure):
         ("n_groups", ctypes.c_int), ("topk_groups", ctypes.c_int), ("gamma", ctypes.c_float),
         ("fp8", ctypes.c_int), ("centroids", ctypes.c_void_p), ("centroid_dtype", ctypes.c_int),
         ("bias", ctypes.c_void_p), ("w13", ctypes.c_void_p), ("w13_scales", ctypes.c_void_p),
-        ("w2", ctypes.c_void_p), ("w2_scales", ctypes.c_void_p),
+        ("w2", ctypes.c_void_p), ("w2_scales", ctypes.c_void_p), ("centroids_prepared", ctypes.c_void_p),
     ]
 
 
@@ -80,6 +82,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "fp8_quant_128x128": (i32, [vp, i64, i64, vp, vp, vp]),
         "moe_route_workspace_size": (sz, [i64, i32, i32, i32]),
         "moe_route": (i32, [vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
+        "moe_route_prepared_centroids_size": (sz, [i32, i32, i32]),
+        "moe_route_prepare_centroids": (i32, [vp, i32, i32, i32, vp, sz, vp]),
+        "moe_route_prepared_workspace_size": (sz, [i64, i32, i32, i32]),
+        "moe_route_prepared": (i32, [vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
         "moe_permute_workspace_size": (sz, [i64, i32]),
         "moe_permute": (i32, [vp, i64, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_permute_static": (i32, [vp, i64, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
@@ -179,6 +185,40 @@ def moe_route(u, centroids, bias, K, n_groups=1, topk_groups=1, want_scores=Fals
     ws = _ws(need, dev) if workspace is None else workspace
     _check(L.moe_route(_p(u), T, d, _p(centroids), cdt, _p(bias), N, K, n_groups, topk_groups, _p(idx), _p(gates),
                        _p(loads), _p(scores), _p(ws), ws.numel(), _stream()), "moe_route")
+    return idx, gates, loads, scores
+
+
+def moe_route_prepare_centroids(centroids, prepared=None):
+    """-> the gate's tensor-core operand for these centroids (uint8 device buffer),
+    to pass to moe_route_prepared while the centroids stay the same."""
+    _require_cuda()
+    L = load_library()
+    N, d = centroids.shape
+    cdt = MOE_DTYPE_F32 if centroids.dtype == torch.float32 else MOE_DTYPE_BF16
+    need = L.moe_route_prepared_centroids_size(d, N, cdt)
+    prepared = _ws(need, centroids.device) if prepared is None else prepared
+    _check(L.moe_route_prepare_centroids(_p(centroids), cdt, N, d, _p(prepared), prepared.numel(), _stream()),
+           "moe_route_prepare_centroids")
+    return prepared
+
+
+def moe_route_prepared(u, prepared, centroid_dtype, N, bias, K, n_groups=1, topk_groups=1, want_scores=False,
+                       workspace=None):
+    """moe_route from prepared centroids (centroid_dtype: MOE_DTYPE_F32 / MOE_DTYPE_BF16 of the
+    centroids they came from) -> (topk_idx, gates, loads, scores or None)."""
+    _require_cuda()
+    L = load_library()
+    T, d = u.shape
+    dev = u.device
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    gates = torch.empty((T, K), dtype=torch.float32, device=dev)
+    loads = torch.empty((N,), dtype=torch.int32, device=dev)
+    scores = torch.empty((T, N), dtype=torch.float32, device=dev) if want_scores else None
+    need = L.moe_route_prepared_workspace_size(T, d, N, centroid_dtype)
+    ws = _ws(need, dev) if workspace is None else workspace
+    _check(L.moe_route_prepared(_p(u), T, d, _p(prepared), centroid_dtype, _p(bias), N, K, n_groups, topk_groups,
+                                _p(idx), _p(gates), _p(loads), _p(scores), _p(ws), ws.numel(), _stream()),
+           "moe_route_prepared")
     return idx, gates, loads, scores
 
 

@@ -12,12 +12,14 @@ namespace moe {
 
 
 int num_sms() {
-    static int n = 0;
+    // SM count of the current device, looked up once per device
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int n = cache[dev].load(std::memory_order_relaxed);
     if (n <= 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
     return n;
 }
@@ -129,6 +131,46 @@ size_t moe_route_workspace_size(int64_t T, int d, int N, int centroid_dtype) {
     return moe::plan_route(T, d, N, centroid_dtype).total_bytes;
 }
 
+size_t moe_route_prepared_centroids_size(int d, int N, int centroid_dtype) {
+    return moe::prepared_centroid_bytes(d, N, centroid_dtype);
+}
+
+size_t moe_route_prepared_workspace_size(int64_t T, int d, int N, int centroid_dtype) {
+    return moe::plan_route(T, d, N, centroid_dtype).zpart_bytes;
+}
+
+moe_status moe_route_prepare_centroids(const void* centroids, int centroid_dtype, int N, int d, void* prepared,
+                                       size_t prepared_bytes, moe_stream_t stream) {
+    REQUIRE(d > 0 && d % 64 == 0, "moe_route_prepare_centroids: d=%d must be a positive multiple of 64", d);
+    REQUIRE(N >= 1 && N <= 1024, "moe_route_prepare_centroids: N=%d must be in [1, 1024]", N);
+    REQUIRE(centroid_dtype == MOE_DTYPE_F32 || centroid_dtype == MOE_DTYPE_BF16,
+            "moe_route_prepare_centroids: centroid dtype %d", centroid_dtype);
+    REQUIRE(centroids && prepared, "moe_route_prepare_centroids: null pointer");
+    const moe::RoutePlan plan = moe::plan_route(0, d, N, centroid_dtype);
+    if (prepared_bytes < plan.split_bytes || (reinterpret_cast<uintptr_t>(prepared) & 255u))
+        return fail(MOE_ERR_WORKSPACE, "moe_route_prepare_centroids: needs %zu bytes, 256-byte aligned",
+                    plan.split_bytes);
+    CUDA_OK(moe::launch_route_prepare(centroids, centroid_dtype, N, d, plan, prepared, stream));
+    return MOE_OK;
+}
+
+moe_status moe_route_prepared(const uint16_t* u, int64_t T, int d, const void* prepared, int centroid_dtype,
+                              const float* bias, int N, int K, int n_groups, int topk_groups, int32_t* topk_idx,
+                              float* gates, int32_t* loads, float* scores, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream) {
+    STATUS_OK(check_route(u, T, d, prepared, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates,
+                          loads));
+    const moe::RoutePlan plan = moe::plan_route(T, d, N, centroid_dtype);
+    if (T > 0 && (reinterpret_cast<uintptr_t>(prepared) & 255u))
+        return fail(MOE_ERR_INVALID_ARG, "moe_route_prepared: prepared centroids must be 256-byte aligned");
+    if (T > 0 && (!workspace || workspace_bytes < plan.zpart_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return fail(MOE_ERR_WORKSPACE, "moe_route_prepared: workspace needs %zu bytes, 256-byte aligned",
+                    plan.zpart_bytes);
+    CUDA_OK(moe::launch_route(u, T, d, prepared, bias, N, K, n_groups > 1 ? n_groups : 1,
+                              n_groups > 1 ? topk_groups : 1, topk_idx, gates, loads, scores, workspace, plan, stream));
+    return MOE_OK;
+}
+
 moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype, const float* bias,
                      int N, int K, int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
                      float* scores, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
@@ -137,8 +179,10 @@ moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids,
     const moe::RoutePlan plan = moe::plan_route(T, d, N, centroid_dtype);
     if (!workspace || workspace_bytes < plan.total_bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return fail(MOE_ERR_WORKSPACE, "moe_route: workspace needs %zu bytes, 256-byte aligned", plan.total_bytes);
-    CUDA_OK(moe::launch_route(u, T, d, centroids, centroid_dtype, bias, N, K, n_groups > 1 ? n_groups : 1,
-                              n_groups > 1 ? topk_groups : 1, topk_idx, gates, loads, scores, workspace, plan, stream));
+    uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+    if (T > 0) CUDA_OK(moe::launch_route_prepare(centroids, centroid_dtype, N, d, plan, ws, stream));
+    CUDA_OK(moe::launch_route(u, T, d, ws, bias, N, K, n_groups > 1 ? n_groups : 1, n_groups > 1 ? topk_groups : 1,
+                              topk_idx, gates, loads, scores, ws + plan.split_bytes, plan, stream));
     return MOE_OK;
 }
 
@@ -290,7 +334,8 @@ LayerWs layer_ws(const moe_layer_weights* w, int64_t T, int host_slots) {
         o += up256(bytes);
         return at;
     };
-    L.route = take(moe::plan_route(T, w->d, w->N, w->centroid_dtype).total_bytes);
+    const moe::RoutePlan rp = moe::plan_route(T, w->d, w->N, w->centroid_dtype);
+    L.route = take(w->centroids_prepared ? rp.zpart_bytes : rp.total_bytes);
     L.perm = take(moe::permute_ws_bytes(T, w->N));
     L.offsets = take(size_t(w->N + 2) * 4);
     L.perm_token = take(size_t(T) * w->K * 4);
@@ -350,8 +395,13 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
         return MOE_OK;
     };
     STATUS_OK(mark(0));
-    STATUS_OK(moe_route(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups, topk,
-                        gates, loads, nullptr, ws + L.route, L.perm - L.route, stream));
+    if (w->centroids_prepared)
+        STATUS_OK(moe_route_prepared(u, T, d, w->centroids_prepared, w->centroid_dtype, w->bias, N, K, w->n_groups,
+                                     w->topk_groups, topk, gates, loads, nullptr, ws + L.route, L.perm - L.route,
+                                     stream));
+    else
+        STATUS_OK(moe_route(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups,
+                            topk, gates, loads, nullptr, ws + L.route, L.perm - L.route, stream));
     STATUS_OK(mark(1));
     STATUS_OK(moe_permute(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
                           reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,

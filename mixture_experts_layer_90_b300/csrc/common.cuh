@@ -7,6 +7,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -272,5 +275,41 @@ __device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
 
 // fp32 scale of a 1x128 tile from its amax: amax / 448, or 1 for a zero tile.
 __device__ __forceinline__ float tile_scale(float amax) { return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f); }
+
+// ---------------------------------------------------------------------------
+// Host: set-up that a kernel needs once on each device (function attributes
+// such as the dynamic shared-memory limit are per device). Thread-safe: the
+// first caller on a device runs `fn`; callers racing with it wait for it.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+struct PerDeviceOnce {
+    std::atomic<uint64_t> done{0};
+    std::mutex m;
+};
+
+template <class Fn>
+cudaError_t once_per_device(PerDeviceOnce& once, Fn&& fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const uint64_t bit = uint64_t(1) << dev;
+    if (once.done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(once.m);
+    if (once.done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    e = fn();
+    if (e == cudaSuccess) once.done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device.
+template <class K>
+cudaError_t allow_smem(PerDeviceOnce& once, K* kernel, int bytes) {
+    return once_per_device(once, [&] {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+}
 
 }  // namespace moe

@@ -236,7 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sa_src[i] = args.sa + r;
                 }
                 const float* sb_src = args.sb + (int64_t(it.g) * (args.Nd / 128) + 2 * it.nt) * nkb;
-                for (int ks = 0; ks < nkb; ++ks) {
+                // the same K blocks as the MMA warp and the epilogue: this split's own
+                const int k0 = it.sp * steps_per_split;
+                const int k1 = min(args.k_steps, k0 + steps_per_split);
+                for (int ks = k0; ks < k1; ++ks) {
                     int ok = 1;
                     if (lane == 0) ok = mbar_wait(smem_u32(&s.sempty[sslot]), sphase ^ 1u, abort);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -262,35 +265,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ---------------- tcgen05.mma issuer ----------------
-        constexpr uint32_t idesc = kMode == kModeFP8 ? make_idesc(0, 0, kBM, kBN) : make_idesc(1, 1, kBM, kBN);
-        const int P = kMode == kModeFP8 ? 1 : args.promote_steps;
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t acc_iter = 0;
-        for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
-            Item it = decode(item, s, G, n_tiles_n, splits);
-            const int k0 = it.sp * steps_per_split;
-            const int k1 = min(args.k_steps, k0 + steps_per_split);
-            uint32_t buf = acc_iter & 1u;
-            bool ok = true;
-            for (int ks = k0; ks < k1; ++ks) {
-                // one TMEM partial per chunk of P K steps (FP8: every 128-K block)
-                const bool first = (ks - k0) % P == 0;
-                const bool last = (ks - k0) % P == P - 1 || ks == k1 - 1;
-                if (first) {
-                    buf = acc_iter & 1u;
-                    if (!mbar_wait(smem_u32(&s.tempty[buf]), ((acc_iter >> 1) & 1u) ^ 1u, abort)) {
+        // ---------------- tcgen05.mma issuer: lane 0 alone ----------------
+        // Only lane 0 waits and issues, so a wait that gives up cannot split the warp.
+        if (lane == 0) {
+            constexpr uint32_t idesc = kMode == kModeFP8 ? make_idesc(0, 0, kBM, kBN) : make_idesc(1, 1, kBM, kBN);
+            const int P = kMode == kModeFP8 ? 1 : args.promote_steps;
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t acc_iter = 0;
+            for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
+                Item it = decode(item, s, G, n_tiles_n, splits);
+                const int k0 = it.sp * steps_per_split;
+                const int k1 = min(args.k_steps, k0 + steps_per_split);
+                uint32_t buf = acc_iter & 1u;
+                bool ok = true;
+                for (int ks = k0; ks < k1; ++ks) {
+                    // one TMEM partial per chunk of P K steps (FP8: every 128-K block)
+                    const bool first = (ks - k0) % P == 0;
+                    const bool last = (ks - k0) % P == P - 1 || ks == k1 - 1;
+                    if (first) {
+                        buf = acc_iter & 1u;
+                        if (!mbar_wait(smem_u32(&s.tempty[buf]), ((acc_iter >> 1) & 1u) ^ 1u, abort)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!mbar_wait(smem_u32(&s.full[stage]), phase, abort)) {
                         ok = false;
                         break;
                     }
-                }
-                if (!mbar_wait(smem_u32(&s.full[stage]), phase, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
+                    tc_fence_after();
                     const uint64_t ad = smem_desc_sw128(ringA + stage * kABytes);
                     const uint64_t bd = smem_desc_sw128(ringB + stage * kBBytes);
                     const uint32_t d = tmem_base + buf * kBN;
@@ -301,19 +305,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         else mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, acc);
                     }
                     tc_commit(smem_u32(&s.empty[stage]));
-                    if (last) tc_commit(smem_u32(&s.tfull[buf]));
+                    if (last) {
+                        tc_commit(smem_u32(&s.tfull[buf]));
+                        acc_iter += 1;
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
-                __syncwarp();
-                if (last) acc_iter += 1;
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                if (!ok) break;
             }
-            if (!ok) break;
-        }
-        // every issued MMA must be complete before TMEM is freed
-        if (lane == 0) {
+            // every issued MMA must be complete before TMEM is freed
             tc_commit(smem_u32(&s.drain));
             mbar_wait_limit(smem_u32(&s.drain), 0, 200000000ull);
         }
@@ -348,22 +351,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) acc2[i] = make_float2(0.0f, 0.0f);
                 for (int ks = k0; ks < k1; ++ks) {
-                    if (!mbar_wait(smem_u32(&s.sfull[sslot]), sphase, abort)) {
-                        ok = false;
-                        break;
+                    bool got = mbar_wait(smem_u32(&s.sfull[sslot]), sphase, abort);
+                    float fl = 0.0f, fh = 0.0f;
+                    if (got) {
+                        const float sa_v = s.scales[sslot].sa[row_in_tile];
+                        fl = sa_v * s.scales[sslot].sb[0];
+                        fh = sa_v * s.scales[sslot].sb[1];
+                        // each lane releases the slot after its own reads (no warp barrier and
+                        // no single-lane branch in the promotion loop)
+                        mbar_arrive(smem_u32(&s.sempty[sslot]));
                     }
-                    const float sa_v = s.scales[sslot].sa[row_in_tile];
-                    const float fl = sa_v * s.scales[sslot].sb[0];
-                    const float fh = sa_v * s.scales[sslot].sb[1];
-                    // each lane releases the slot after its own reads (no warp barrier and
-                    // no single-lane branch in the promotion loop)
-                    mbar_arrive(smem_u32(&s.sempty[sslot]));
                     if (++sslot == kSSlots) {
                         sslot = 0;
                         sphase ^= 1u;
                     }
                     const uint32_t buf = acc_iter & 1u;
-                    if (!mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort)) {
+                    got = got && mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort);
+                    // the TMEM loads below are warp-collective: the warp goes on only if
+                    // every lane saw both waits complete, and gives up as one otherwise
+                    if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
                     }
@@ -404,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 32; ++i) acc2[i] = make_float2(0.0f, 0.0f);
                 for (int c0 = k0; c0 < k1; c0 += P) {
                     const uint32_t buf = acc_iter & 1u;
-                    if (!mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort)) {
+                    const bool got = mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort);
+                    if (!__all_sync(0xffffffffu, got)) {   // warp-collective TMEM loads follow
                         ok = false;
                         break;
                     }
@@ -454,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t par = tile_iter & 1u;
                     s.amax[par][wg][row_in_tile] = amax;
                     mbar_arrive(smem_u32(&s.xchg[par]));
-                    if (!mbar_wait(smem_u32(&s.xchg[par]), (tile_iter >> 1) & 1u, abort)) break;
+                    const bool got = mbar_wait(smem_u32(&s.xchg[par]), (tile_iter >> 1) & 1u, abort);
+                    if (!__all_sync(0xffffffffu, got)) break;   // the warp leaves the tile loop as one
                     amax = fmaxf(fmaxf(s.amax[par][0][row_in_tile], s.amax[par][1][row_in_tile]),
                                  fmaxf(s.amax[par][2][row_in_tile], s.amax[par][3][row_in_tile]));
                     const float sc = tile_scale(amax);
@@ -575,13 +583,9 @@ bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inne
 template <int kMode, int kEpi>
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
                           cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kMode, kEpi>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDeviceOnce once;
+    cudaError_t e = allow_smem(once, grouped_gemm_kernel<kMode, kEpi>, int(kSmemBytes));
+    if (e != cudaSuccess) return e;
     grouped_gemm_kernel<kMode, kEpi><<<grid, kThreads, kSmemBytes, stream>>>(a, b, args);
     return cudaGetLastError();
 }

@@ -14,18 +14,21 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t rows, int64_t cols, uint8_t* q, float* scales,
                                  cudaStream_t stream);
 
-// Routing: bf16 split of the centroids, tensor-core gate logits, selection.
+// Routing: bf16 split of the centroids (prepared once per set of centroids),
+// tensor-core gate logits, selection.
 struct RoutePlan {
     int terms;      // 3 for fp32 centroids (exact bf16 split), 1 for bf16
     int n_pad;      // N rounded up to 256
     int splits;     // split-K parts of the gate GEMM
     size_t split_bytes, zpart_bytes, total_bytes;
 };
+size_t prepared_centroid_bytes(int d, int N, int centroid_dtype);
 RoutePlan plan_route(int64_t T, int d, int N, int centroid_dtype);
-cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype,
-                         const float* bias, int N, int K, int n_groups, int topk_groups, int32_t* topk_idx,
-                         float* gates, int32_t* loads, float* scores, void* ws, const RoutePlan& plan,
-                         cudaStream_t stream);
+cudaError_t launch_route_prepare(const void* centroids, int centroid_dtype, int N, int d, const RoutePlan& plan,
+                                 void* prepared, cudaStream_t stream);
+cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* prepared, const float* bias, int N, int K,
+                         int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
+                         float* scores, void* zpart_ws, const RoutePlan& plan, cudaStream_t stream);
 
 // Permutation (stable counting sort by expert) and row scatter.
 size_t permute_ws_bytes(int64_t T, int N);

@@ -240,13 +240,8 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
         int64_t blocks = (n_chunks + 7) / 8;
         if (blocks > cap) blocks = cap;
         const size_t smem = size_t(N + 1) * 4 + size_t(8) * N * 4;
-        static bool configured = false;
-        if (!configured) {
-            if ((e = cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024)) !=
-                cudaSuccess)
-                return e;
-            configured = true;
-        }
+        static PerDeviceOnce once;
+        if ((e = allow_smem(once, perm_rank_kernel, 64 * 1024)) != cudaSuccess) return e;
         perm_rank_kernel<<<int(blocks), 256, smem, stream>>>(topk_idx, T, N, K, counts, totals, with_shared, offsets,
                                                              perm_token, dest_row);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -15,7 +15,9 @@
 // array's name as a device address (it is a host-side stand-in), so the
 // first call on each device looks up the real address with
 // cudaGetSymbolAddress while that device is current, and later calls on that
-// device reuse it.
+// device reuse it. The cached address belongs to the context it was looked up
+// in: it is dropped when a launch fails, and a caller that resets the device
+// (cudaDeviceReset) must not call this entry point again in that process.
 #include <mutex>
 
 #include "common.cuh"
@@ -29,7 +31,6 @@ constexpr int64_t kStaticScratchInts = int64_t(1) << 20;   // 4 MiB of int32
 
 __device__ __align__(256) int32_t g_permute_scratch[kStaticScratchInts];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
 
@@ -51,6 +52,15 @@ void* static_scratch(cudaError_t* err) {
         g_scratch_addr[dev] = p;
     }
     return g_scratch_addr[dev];
+}
+
+// Forgets the current device's cached address, so that the next call looks it
+// up again (after a failed launch, the context may have been torn down).
+void forget_static_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    g_scratch_addr[dev] = nullptr;
 }
 
 }  // namespace
@@ -84,7 +94,11 @@ extern "C" moe_status moe_permute_static(const uint16_t* x, int64_t T, int d, co
     cudaError_t e = cudaSuccess;
     void* scratch = moe::static_scratch(&e);
     if (!scratch) return fail(MOE_ERR_CUDA, "moe_permute_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    CUDA_OK(moe::launch_permute(x, T, d, topk_idx, N, K, out_dtype, with_shared ? 1 : 0, offsets, perm_token,
-                                dest_row, x_perm, x_perm_scales, scratch, stream));
+    e = moe::launch_permute(x, T, d, topk_idx, N, K, out_dtype, with_shared ? 1 : 0, offsets, perm_token, dest_row,
+                            x_perm, x_perm_scales, scratch, stream);
+    if (e != cudaSuccess) {
+        moe::forget_static_scratch();
+        return fail(MOE_ERR_CUDA, "moe_permute_static: launch: %s", cudaGetErrorString(e));
+    }
     return MOE_OK;
 }

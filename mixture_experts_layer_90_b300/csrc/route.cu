@@ -92,6 +92,9 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
 
     for (int64_t t = int64_t(blockIdx.x) * 8 + w; t < T; t += int64_t(gridDim.x) * 8) {
         float s[J], key[J];
+        // bit j: expert 32j + lane is out of the running (past N, outside the kept
+        // groups, or already chosen)
+        uint32_t excl = 0;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int i = 32 * j + lane;
@@ -100,9 +103,14 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
                 const float* zp = zpart + t * n_pad + i;
                 z = __ldg(zp);
                 for (int p = 1; p < splits; ++p) z += __ldg(zp + p * plane);
+            } else {
+                excl |= 1u << j;
             }
             s[j] = __fdiv_rn(1.0f, 1.0f + expf(-z));
-            key[j] = i < N ? s[j] + b[j] : -INFINITY;
+            const float kv = s[j] + b[j];
+            // a NaN key (NaN token or bias) ranks below every number: it can still be
+            // chosen, last, so every token keeps exactly K valid experts
+            key[j] = (i < N && kv == kv) ? kv : -INFINITY;
             if (scores && i < N) scores[t * N + i] = s[j];
         }
         if (n_groups > 1) {
@@ -126,43 +134,53 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
                     }
                 }
                 gscore = t1 + t2;
+                if (!(gscore == gscore)) gscore = -INFINITY;   // +inf + -inf
             }
             __syncwarp();
+            // topk_groups rounds over the groups not kept yet; a lane past n_groups or
+            // holding a kept group offers no candidate, so every round keeps a new group
             uint32_t keep = 0;
+            bool kept_me = false;
             for (int r = 0; r < topk_groups; ++r) {
-                float v = gscore;
-                int gi = lane < n_groups ? lane : 0x7fffffff;
+                const bool cand = lane < n_groups && !kept_me;
+                float v = cand ? gscore : -INFINITY;
+                int gi = cand ? lane : 0x7fffffff;
                 warp_argmax(v, gi);
-                keep |= 1u << gi;
-                if (lane == gi) gscore = -INFINITY;
+                if (gi < n_groups) {
+                    keep |= 1u << gi;
+                    if (lane == gi) kept_me = true;
+                }
             }
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 const int i = 32 * j + lane;
-                if (i < N && !((keep >> (i / per_group)) & 1u)) key[j] = -INFINITY;
+                if (i < N && !((keep >> (i / per_group)) & 1u)) excl |= 1u << j;
             }
         }
         int my_id = 0;
         float my_s = 0.0f;
         for (int k = 0; k < K; ++k) {
+            // each lane offers its best expert still in the running (the lowest such
+            // index when keys tie or are all -inf); lanes with none offer id 0x7fffffff
             float v = -INFINITY;
             int id = 0x7fffffff;
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 const int i = 32 * j + lane;
-                if (key[j] > v) {   // j ascending: ties inside a lane keep the lower index
+                if (!((excl >> j) & 1u) && (id == 0x7fffffff || key[j] > v)) {
                     v = key[j];
                     id = i;
                 }
             }
             warp_argmax(v, id);
+            // id < N: at most k < K <= (experts in the running) were taken before
             const int wl = id & 31, wj = id >> 5;
             float sv = 0.0f;
 #pragma unroll
             for (int j = 0; j < J; ++j)
                 if (j == wj) {
                     sv = s[j];
-                    if (lane == wl) key[j] = -INFINITY;
+                    if (lane == wl) excl |= 1u << j;
                 }
             sv = __shfl_sync(0xffffffffu, sv, wl);
             if (lane == k) {
@@ -185,7 +203,8 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
         if (lane < K) {
             topk_idx[t * K + rank] = my_id;
             gates[t * K + rank] = __fdiv_rn(my_s, den);
-            atomicAdd(&hist[my_id], 1);
+            if (my_id >= 0 && my_id < N) atomicAdd(&hist[my_id], 1);
+            else report(MOE_ERR_DEVICE_DATA);
         }
     }
     __syncthreads();
@@ -198,13 +217,9 @@ cudaError_t launch_select(const float* zpart, int splits, int64_t T, int n_pad, 
                           int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
                           float* scores, cudaStream_t stream) {
     const size_t smem = size_t(N) * 4 + (n_groups > 1 ? size_t(8) * N * 4 : 0);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(route_select_kernel<J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             48 * 1024);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDeviceOnce once;
+    cudaError_t e = allow_smem(once, route_select_kernel<J>, 48 * 1024);
+    if (e != cudaSuccess) return e;
     int64_t blocks = (T + 7) / 8;
     const int64_t cap = int64_t(num_sms()) * 8;
     if (blocks > cap) blocks = cap;
@@ -214,6 +229,12 @@ cudaError_t launch_select(const float* zpart, int splits, int64_t T, int n_pad, 
 }
 
 }  // namespace
+
+size_t prepared_centroid_bytes(int d, int N, int centroid_dtype) {
+    const size_t terms = centroid_dtype == MOE_DTYPE_F32 ? 3 : 1;
+    const size_t n_pad = size_t(N + 255) / 256 * 256;
+    return (n_pad * terms * size_t(d) * 2 + 255) / 256 * 256;
+}
 
 RoutePlan plan_route(int64_t T, int d, int N, int centroid_dtype) {
     RoutePlan p{};
@@ -242,28 +263,29 @@ RoutePlan plan_route(int64_t T, int d, int N, int centroid_dtype) {
         }
     }
     p.splits = best;
-    p.split_bytes = (size_t(p.n_pad) * p.terms * d * 2 + 255) / 256 * 256;
+    p.split_bytes = prepared_centroid_bytes(d, N, centroid_dtype);
     p.zpart_bytes = (size_t(p.splits) * size_t(T) * p.n_pad * 4 + 255) / 256 * 256;
     p.total_bytes = p.split_bytes + p.zpart_bytes;
     return p;
 }
 
-cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype,
-                         const float* bias, int N, int K, int n_groups, int topk_groups, int32_t* topk_idx,
-                         float* gates, int32_t* loads, float* scores, void* ws, const RoutePlan& plan,
-                         cudaStream_t stream) {
+cudaError_t launch_route_prepare(const void* centroids, int centroid_dtype, int N, int d, const RoutePlan& plan,
+                                 void* prepared, cudaStream_t stream) {
+    const int64_t total = int64_t(plan.n_pad) * d;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > int64_t(num_sms()) * 16) blocks = int64_t(num_sms()) * 16;
+    split_centroids_kernel<<<int(blocks), 256, 0, stream>>>(centroids, centroid_dtype == MOE_DTYPE_F32, N, plan.n_pad,
+                                                            d, plan.terms, reinterpret_cast<uint16_t*>(prepared));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* prepared, const float* bias, int N, int K,
+                         int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
+                         float* scores, void* zpart_ws, const RoutePlan& plan, cudaStream_t stream) {
     cudaError_t e = cudaMemsetAsync(loads, 0, sizeof(int32_t) * N, stream);
     if (e != cudaSuccess || T == 0) return e;
-    uint16_t* esplit = reinterpret_cast<uint16_t*>(ws);
-    float* zpart = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + plan.split_bytes);
-    {
-        const int64_t total = int64_t(plan.n_pad) * d;
-        int64_t blocks = (total + 255) / 256;
-        if (blocks > int64_t(num_sms()) * 16) blocks = int64_t(num_sms()) * 16;
-        split_centroids_kernel<<<int(blocks), 256, 0, stream>>>(centroids, centroid_dtype == MOE_DTYPE_F32, N,
-                                                                plan.n_pad, d, plan.terms, esplit);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    const uint16_t* esplit = reinterpret_cast<const uint16_t*>(prepared);
+    float* zpart = reinterpret_cast<float*>(zpart_ws);
     CUtensorMap ta, tb;
     if (!make_kmajor_map(&ta, u, true, uint64_t(d), uint64_t(T), uint64_t(d) * 2, 128) ||
         !make_kmajor_map(&tb, esplit, true, uint64_t(plan.terms) * d, uint64_t(plan.n_pad),

@@ -18,7 +18,7 @@ import ctypes
 import torch
 
 from . import (MOE_DTYPE_BF16, MOE_DTYPE_F32, LayerOutputs, LayerWeights, _check, _p, _require_cuda, _stream,
-               fp8_quant_128x128, load_library)
+               fp8_quant_128x128, load_library, moe_route_prepare_centroids)
 
 
 def interleave_gate_up(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
@@ -36,13 +36,16 @@ class MoELayer:
         self.fp8 = w13.dtype == torch.uint8
         self.centroids, self.bias = centroids, bias
         self.w13, self.w2, self.w13_scales, self.w2_scales = w13, w2, w13_scales, w2_scales
+        # the gate's operand is prepared once: the centroids stay fixed, only the bias moves
+        self.centroids_prepared = moe_route_prepare_centroids(centroids)
         self._desc = LayerWeights(
             d=d, N=N, K=K, I=I, n_groups=n_groups, topk_groups=topk_groups, gamma=gamma, fp8=int(self.fp8),
             centroids=centroids.data_ptr(),
             centroid_dtype=MOE_DTYPE_F32 if centroids.dtype == torch.float32 else MOE_DTYPE_BF16,
             bias=bias.data_ptr(), w13=w13.data_ptr(),
             w13_scales=w13_scales.data_ptr() if w13_scales is not None else None,
-            w2=w2.data_ptr(), w2_scales=w2_scales.data_ptr() if w2_scales is not None else None)
+            w2=w2.data_ptr(), w2_scales=w2_scales.data_ptr() if w2_scales is not None else None,
+            centroids_prepared=self.centroids_prepared.data_ptr())
         self._ws = {}
         self.loads = torch.zeros((N,), dtype=torch.int32, device=centroids.device)
 
@@ -71,6 +74,10 @@ class MoELayer:
                 w13[e].copy_(w13e)
                 w2[e].copy_(w2e)
         return cls(d, N, K, I, centroids, bias, w13, w2, s13, s2, **kw)
+
+    def prepare_centroids(self):
+        """Re-prepares the gate's operand; call after changing self.centroids in place."""
+        moe_route_prepare_centroids(self.centroids, self.centroids_prepared)
 
     def workspace(self, T: int, host=False) -> torch.Tensor:
         """host: False (device buffers), True (host-buffer call) or "pipeline"."""

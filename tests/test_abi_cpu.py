@@ -152,3 +152,32 @@ def test_wait_self_test_limit_is_bounded(L):
     s = ctypes.c_void_p(0)
     assert L.moe_selftest_wait_timeout(0, s) == M.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_wait_timeout(2_000_000_000, s) == M.MOE_ERR_INVALID_ARG
+
+
+def test_prepared_routing_checks_its_arguments(L):
+    p, s = _ok_ptr(), ctypes.c_void_p(0)
+    need = L.moe_route_prepared_centroids_size(7168, 256, M.MOE_DTYPE_F32)
+    assert need == 256 * 3 * 7168 * 2                  # three bf16 terms per fp32 centroid value
+    assert L.moe_route_prepared_centroids_size(256, 16, M.MOE_DTYPE_BF16) == 256 * 256 * 2   # rows padded to 256
+    prep = lambda *a: L.moe_route_prepare_centroids(*a)  # noqa: E731
+    assert prep(p, M.MOE_DTYPE_F32, 256, 100, p, need, s) == M.MOE_ERR_INVALID_ARG       # d % 64
+    assert prep(p, M.MOE_DTYPE_F32, 2048, 128, p, need, s) == M.MOE_ERR_INVALID_ARG      # N > 1024
+    assert prep(p, M.MOE_DTYPE_E4M3, 256, 128, p, need, s) == M.MOE_ERR_INVALID_ARG      # dtype
+    assert prep(None, M.MOE_DTYPE_F32, 256, 128, p, need, s) == M.MOE_ERR_INVALID_ARG
+    small = L.moe_route_prepared_centroids_size(128, 256, M.MOE_DTYPE_F32)
+    assert prep(p, M.MOE_DTYPE_F32, 256, 128, p, small - 1, s) == M.MOE_ERR_WORKSPACE
+    assert prep(p, M.MOE_DTYPE_F32, 256, 128, ctypes.c_void_p(4096 + 16), small, s) == M.MOE_ERR_WORKSPACE
+    # routing from a prepared operand: the same rules as moe_route, a smaller workspace
+    ws = L.moe_route_prepared_workspace_size(1000, 1024, 256, M.MOE_DTYPE_F32)
+    assert ws < L.moe_route_workspace_size(1000, 1024, 256, M.MOE_DTYPE_F32)
+    call = lambda T, d, N, K, ws_bytes, prepared=p: L.moe_route_prepared(  # noqa: E731
+        p, T, d, prepared, M.MOE_DTYPE_F32, p, N, K, 1, 1, p, p, p, None, p, ws_bytes, s)
+    assert call(1000, 100, 256, 8, ws) == M.MOE_ERR_INVALID_ARG
+    assert call(1000, 1024, 256, 17, ws) == M.MOE_ERR_INVALID_ARG
+    assert call(1000, 1024, 256, 8, ws - 1) == M.MOE_ERR_WORKSPACE
+    assert call(1000, 1024, 256, 8, ws, prepared=ctypes.c_void_p(4096 + 16)) == M.MOE_ERR_INVALID_ARG
+    # a layer given prepared centroids needs no room for them in its workspace
+    w = _v3_weights()
+    plain = L.moe_layer_workspace_size(ctypes.byref(w), 8192)
+    w.centroids_prepared = 4096
+    assert L.moe_layer_workspace_size(ctypes.byref(w), 8192) <= plain - 256 * 3 * 7168 * 2

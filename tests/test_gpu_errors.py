@@ -82,3 +82,57 @@ def test_combine_reports_out_of_range_rows():
     m.moe_combine(u, y[T * K:], y, g, dest)
     assert m.device_status() == m.MOE_ERR_DEVICE_DATA
     _context_still_works()
+
+
+def _route_valid(idx, N, K):
+    """Every token has K distinct expert ids in [0, N), ascending."""
+    idx = idx.cpu().numpy()
+    assert idx.shape[1] == K
+    assert ((idx >= 0) & (idx < N)).all()
+    assert (np.diff(idx, axis=1) > 0).all()
+    return idx
+
+
+@pytest.mark.parametrize("n_groups,topk_groups", [(1, 1), (8, 3)])
+def test_route_nan_tokens_and_minus_inf_bias_keep_valid_ids(n_groups, topk_groups):
+    """A NaN in a token makes all of its affinities NaN, and a -inf bias makes an
+    expert's key -inf; neither may produce an expert id outside [0, N) (the
+    selection ranks NaN keys last, ties to the lower index). The other tokens are
+    routed as usual and the loads match the ids."""
+    m = _lib()
+    T, d, N, K = 64, 256, 64, 6
+    u = S.normal((T, d), 1.0, S.key(0, "nan-u")).clone()
+    u[5, 17] = float("nan")
+    u[40, :] = float("nan")
+    e = S.normal((N, d), 1.0 / 16, S.key(0, "nan-e"), dtype=torch.float32)
+    b = S.uniform((N,), -0.01, 0.01, S.key(0, "nan-b")).clone()
+    b[[0, 3, 9, 33]] = float("-inf")
+    idx, gates, loads, _ = m.moe_route(u.cuda(), e.cuda(), b.cuda(), K, n_groups, topk_groups)
+    assert m.device_status() == m.MOE_OK
+    ids = _route_valid(idx, N, K)
+    np.testing.assert_array_equal(loads.cpu().numpy(), np.bincount(ids.ravel(), minlength=N))
+    # a -inf bias keeps an expert out wherever enough finite keys remain
+    ok_rows = np.setdiff1d(np.arange(T), [5, 40])
+    assert not np.isin(ids[ok_rows], [0, 3, 9, 33]).any()
+    # the same tokens with finite values route exactly as before
+    u2 = u.clone()
+    u2[5, 17] = 0.0
+    u2[40, :] = 0.0
+    idx2, _, _, _ = m.moe_route(u2.cuda(), e.cuda(), b.cuda(), K, n_groups, topk_groups)
+    np.testing.assert_array_equal(ids[ok_rows], idx2.cpu().numpy()[ok_rows])
+    _context_still_works()
+
+
+def test_route_all_minus_inf_bias_still_picks_k_experts():
+    m = _lib()
+    T, d, N, K = 16, 128, 32, 8
+    u = S.normal((T, d), 1.0, S.key(0, "ninf-u"))
+    e = S.normal((N, d), 1.0 / 11, S.key(0, "ninf-e"), dtype=torch.float32)
+    b = torch.full((N,), float("-inf"))
+    idx, _, loads, _ = m.moe_route(u.cuda(), e.cuda(), b.cuda(), K)
+    assert m.device_status() == m.MOE_OK
+    ids = _route_valid(idx, N, K)
+    # every key ties at -inf: the lowest K ids win
+    np.testing.assert_array_equal(ids, np.tile(np.arange(K), (T, 1)))
+    assert loads.sum().item() == T * K
+    _context_still_works()

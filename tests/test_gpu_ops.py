@@ -289,6 +289,25 @@ def test_route_forced_bias():
     assert loads.sum() == 300 * 6
 
 
+@pytest.mark.parametrize("f32,n_groups", [(True, 1), (False, 1), (True, 8)])
+def test_route_prepared_is_bit_identical(f32, n_groups):
+    """moe_route_prepare_centroids + moe_route_prepared give exactly what
+    moe_route gives, on two calls that reuse one prepared operand."""
+    m = lib()
+    N, K = (256, 8) if n_groups > 1 else (64, 6)
+    u, e, b = _route_case(300, 512, N, f32=f32)
+    prepared = m.moe_route_prepare_centroids(cuda(e))
+    cdt = m.MOE_DTYPE_F32 if f32 else m.MOE_DTYPE_BF16
+    for seed in (0, 1):
+        uu = u if seed == 0 else S.normal(u.shape, 1.0, S.key(seed, "route-u2"))
+        a = m.moe_route(cuda(uu), cuda(e), cuda(b), K, n_groups, 4 if n_groups > 1 else 1, want_scores=True)
+        p = m.moe_route_prepared(cuda(uu), prepared, cdt, N, cuda(b), K, n_groups, 4 if n_groups > 1 else 1,
+                                 want_scores=True)
+        status_ok()
+        for x, y in zip(a, p):
+            assert torch.equal(x, y)
+
+
 def test_route_full_size():
     """The route+dispatch workload: T=16384, d=7168, 256 fp32 centroids, top-8."""
     sh = S.ROUTE_V3

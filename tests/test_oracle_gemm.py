@@ -261,3 +261,106 @@ def test_layer_with_zero_down_projections_returns_u():
     for fp8 in (True, False):
         got, _, _ = oracle.layer_tokens(u, cent, bias, sh.K, wts, np.arange(sh.T), fp8=fp8)
         np.testing.assert_array_equal(got, u.double().numpy())
+
+
+# --------------------------------------------------------------------------
+# the bf16 expert path (the tiny layer and bf16_grouped_gemm's SwiGLU epilogue)
+# --------------------------------------------------------------------------
+
+def _bf16_rne(x: np.ndarray) -> np.ndarray:
+    """Single rounding of FP64 values to bf16 (8 significant bits, ties to even),
+    written from the definition: x = m * 2^e with 0.5 <= |m| < 1, so m * 2^8 is
+    rounded to an integer by numpy's round-half-to-even. No subnormal or overflow
+    case arises at these magnitudes."""
+    m, e = np.frexp(np.asarray(x, np.float64))
+    return np.ldexp(np.round(m * 256.0), e - 8)
+
+
+def _bruteforce_bf16_ffn(x, w1, w3, w2, swap_gate_up=False, round_a=True):
+    """SwiGLU expert W2 (silu(W1 x) * W3 x) on bf16 values, products exact in FP64;
+    the intermediate a is rounded once to bf16 (where the bf16 kernels store it)."""
+    xf, w1f, w3f, w2f = (t.double().numpy() for t in (x, w1, w3, w2))
+    h1, h3 = xf @ w1f.T, xf @ w3f.T
+    if swap_gate_up:
+        h1, h3 = h3, h1
+    a = h1 / (1.0 + np.exp(-h1)) * h3
+    if round_a:
+        a = _bf16_rne(a)
+    return a @ w2f.T
+
+
+def _bruteforce_bf16_layer(u, cent, bias, K, weights, **ffn_kw):
+    """The layer formula (nlp-lineage page, "The notation") with bf16 experts,
+    written independently of the oracle: numpy FP64 routing (sigmoid affinity,
+    top-K of s + b by a stable sort, gates s / sum s over the chosen), each expert
+    output rounded once to bf16, then u + shared + sum_k g_k y_k in FP64."""
+    uf = u.double().numpy()
+    s = 1.0 / (1.0 + np.exp(-(uf @ cent.double().numpy().T)))
+    key = s + bias.double().numpy()[None, :]
+    out = uf + _bf16_rne(_bruteforce_bf16_ffn(u, *weights(cent.shape[0]), **ffn_kw))
+    for t in range(uf.shape[0]):
+        chosen = np.sort(np.argsort(-key[t], kind="stable")[:K])
+        g = s[t, chosen] / s[t, chosen].sum()
+        for k, e in enumerate(chosen):
+            out[t] += g[k] * _bf16_rne(_bruteforce_bf16_ffn(u[t:t + 1], *weights(e), **ffn_kw))[0]
+    return out
+
+
+def _bf16_case():
+    sh = S.LayerShape(T=6, d=256, N=8, K=3, I=128, fp8=False, centroid_f32=False, name="bf16-bf")
+    u = S.tokens(sh)
+    cent = S.centroids(sh)
+    bias = S.uniform((sh.N,), -0.5, 0.5, S.key(9, "bf16-bf-bias"))   # wide: a bias leaking into g shows
+    wts = {e: S.expert_weights(sh, e) for e in range(sh.N + 1)}
+    return sh, u, cent, bias, (lambda e: wts[e])
+
+
+def test_bf16_rounding_helper_is_a_single_rne_rounding():
+    """The brute force's own bf16 rounding against exactly representable cases:
+    bf16 values are fixed points, midpoints go to the even neighbour, and any other
+    value goes to the nearer neighbour."""
+    bf = torch.tensor([1.0, 1.0078125, -3.5, 448.0, 2.0 ** -20], dtype=torch.float64)
+    np.testing.assert_array_equal(_bf16_rne(bf.numpy()), bf.numpy())
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties to the even mantissa (1)
+    assert _bf16_rne(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    # 1 + 3 * 2^-8 lies halfway between 1 + 2^-7 and 1 + 2^-6: ties to 1 + 2^-6
+    assert _bf16_rne(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2.0 ** -6
+    assert _bf16_rne(np.array([1.0 + 2.0 ** -8 + 2.0 ** -30]))[0] == 1.0 + 2.0 ** -7
+    # agrees with the oracle's C rounding on values away from fp32 double-rounding cases
+    x = S.normal((4096,), 3.0, S.key(0, "bf16-rne"), dtype=torch.float32).double().numpy() * (1 + 2.0 ** -30)
+    np.testing.assert_array_equal(_bf16_rne(x), oracle.bf16_value(oracle.bf16_round(x)))
+
+
+def test_expert_ffn_bf16_matches_independent_bruteforce():
+    """oracle.expert_ffn_bf16 (FP64 products, a rounded to bf16, y unrounded)
+    against the brute force; a swapped gate/up projection or a missing rounding
+    of a moves the result far beyond the agreement of the two."""
+    sh, u, cent, bias, wts = _bf16_case()
+    w1, w3, w2 = wts(2)
+    got = oracle.expert_ffn_bf16(u, w1, w3, w2)
+    ref = _bruteforce_bf16_ffn(u, w1, w3, w2)
+    scale = np.abs(ref).max()
+    assert np.max(np.abs(got - ref)) <= 1e-12 * scale
+    swapped = _bruteforce_bf16_ffn(u, w1, w3, w2, swap_gate_up=True)
+    unrounded = _bruteforce_bf16_ffn(u, w1, w3, w2, round_a=False)
+    assert np.max(np.abs(swapped - ref)) > 1e-2 * scale
+    assert np.max(np.abs(unrounded - ref)) > 1e-5 * scale
+
+
+def test_layer_bf16_composition_matches_independent_bruteforce():
+    """oracle.layer_tokens(fp8=False): routing, bf16 SwiGLU experts with a and y
+    rounded to bf16, the shared expert with gate 1, the gate-weighted sum, against
+    the brute force above. The wide bias range makes a bias leaking into the gates,
+    a dropped shared expert or a swapped gate/up projection show far above the
+    FP64 summation-order differences the two may have."""
+    sh, u, cent, bias, wts = _bf16_case()
+    got, r, _ = oracle.layer_tokens(u, cent, bias, sh.K, wts, np.arange(sh.T), fp8=False)
+    ref = _bruteforce_bf16_layer(u, cent, bias, sh.K, wts)
+    scale = np.abs(ref - u.double().numpy()).max()
+    assert np.max(np.abs(got - ref)) <= 1e-12 * scale, np.max(np.abs(got - ref)) / scale
+    swapped = _bruteforce_bf16_layer(u, cent, bias, sh.K, wts, swap_gate_up=True)
+    assert np.max(np.abs(swapped - ref)) > 1e-2 * scale
+    # the bias steers the choice here: some token's set differs from the unbiased top-K
+    s = 1.0 / (1.0 + np.exp(-(u.double().numpy() @ cent.double().numpy().T)))
+    unbiased = np.sort(np.argsort(-s, axis=1, kind="stable")[:, :sh.K], axis=1)
+    assert np.any(unbiased != r.topk_idx)
