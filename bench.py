@@ -10,10 +10,16 @@ FP8 E4M3 expert weights resident in HBM with 128x128 scales.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line (rank 0). Multi-GPU (torchrun): replicas, one per GPU,
-no collective on the data path (weak scaling; value = all ranks' tokens / the
-slowest rank's time). `--impl reference` times the FP64 CPU oracle on a
-bounded sample of the same workload on the host cores.
+Prints one JSON line (rank 0). Besides the V3 layer (the headline metric), the
+line carries under "configs" the other workloads of the benchmark, each timed
+alone with L2 flushed before every launch and each with its own roofline and a
+bounded CPU-oracle baseline: the tiny bf16 layer, route + dispatch at
+T=16384, the dense FP8 block-scaled GEMM 4096x4096x7168 and the two
+group-limited decode batches (T=64, T=256) on the V3 layer's weights.
+Multi-GPU (torchrun): replicas, one per GPU, no collective on the data path
+(weak scaling; value = all ranks' tokens / the slowest rank's time).
+`--impl reference` times the FP64 CPU oracle on a bounded sample of the same
+workload on the host cores.
 """
 from __future__ import annotations
 
@@ -33,7 +39,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer fwd tokens/s @V3 shape; FP8 grouped-GEMM % of B300 FP8 peak"
 FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor throughput (4.5 / 2.25 PFLOP/s)
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-KERNELS_PER_STEP = 11        # split, gate GEMM, select | count, scan, rank, scatter | GEMM1 | GEMM2 | combine | bias
+KERNELS_PER_STEP = 10        # gate GEMM, select | count, scan, rank, scatter | GEMM1 | GEMM2 | combine | bias
+ORACLE_TOKENS = 4            # V3-layer tokens per oracle sample (reference arm step and cpu_baseline)
 
 
 def profiled_traffic(name):
@@ -68,7 +75,9 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms; summary()
+    covers the samples taken between mark_start() and mark_stop() (the timed
+    region), or all samples if no mark was set."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -84,23 +93,30 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
             t0 = time.time()
             while not self.lines and time.time() - t0 < 10.0 and self.proc.poll() is None:
                 time.sleep(0.01)
-            self.start = len(self.lines)
         except OSError:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.start = len(self.lines)
+
+    def mark_stop(self):
+        time.sleep(0.05)          # let the sampler report the region's last interval
+        self.stop = len(self.lines)
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
-        self.stop = len(self.lines)
+        if self.stop is None:
+            self.stop = len(self.lines)
         if self.proc:
             self.proc.terminate()
             try:
@@ -111,7 +127,7 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines[getattr(self, "start", 0):getattr(self, "stop", None)]:
+        for ln in self.lines[self.start:self.stop]:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -200,7 +216,7 @@ def run_reference(args):
     sh = S.LAYER_V3
     dev = f"cuda:{local}" if torch.cuda.is_available() else None
     inputs = host_layer_inputs(sh, dev)
-    per_step = max(1, int(os.environ.get("REF_TOKENS_PER_STEP", "1")))
+    per_step = max(1, int(os.environ.get("REF_TOKENS_PER_STEP", str(ORACLE_TOKENS))))
     for i in range(args.warmup):
         oracle_sample_timing(sh, inputs, per_step, seed=1000 + i)
     times, cores = [], 1
@@ -226,6 +242,15 @@ def run_reference(args):
 # --------------------------------------------------------------------------
 # the CUDA path
 # --------------------------------------------------------------------------
+
+def fp8_peak_tflops(pk, region_s):
+    """FP8 dense peak to divide by: 2 x the measured bf16 cuBLAS figure (the
+    nominal FP8 / BF16 ratio), burst for a timed region under 2 s, sustained
+    for a longer one."""
+    if region_s < 2.0:
+        return pk["bf16_tflops"] * FP8_OVER_BF16, "bf16 burst"
+    return pk["bf16_tflops_sustained"] * FP8_OVER_BF16, "bf16 sustained"
+
 
 def run_ours(args):
     import torch
@@ -264,6 +289,7 @@ def run_ours(args):
 
     with ClockSampler(local) as clocks:
         barrier()
+        clocks.mark_start()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
@@ -271,6 +297,7 @@ def run_ours(args):
             layer.forward(u_bufs[i % 2], out, stage_events=events[i])
         t1.record()
         barrier()
+        clocks.mark_stop()
     status = moe.device_status()
     assert status == 0, f"device status {status}"
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dev)
@@ -302,7 +329,7 @@ def run_ours(args):
     value = tokens / (elapsed_ms / 1000.0)
     g1, g2 = layer_flops(sh)
     pk, src = peaks()
-    fp8_peak = pk["bf16_tflops_sustained"] * FP8_OVER_BF16
+    fp8_peak, peak_kind = fp8_peak_tflops(pk, elapsed_ms / 1000.0)
     t1s = stage_ms["gemm1_swiglu"] / 1000.0
     t2s = stage_ms["gemm2"] / 1000.0
     gemm1_tflops = g1 / t1s / 1e12
@@ -318,25 +345,41 @@ def run_ours(args):
                    "l2": "inputs larger than L2: 11.3 GB of FP8 expert weights streamed per step, two "
                          "alternating 117 MB token batches"},
         "fp8_gemm_pct_of_peak": gemm_pct,
+        "gemm2_frac_of_fp8_peak": g2 / t2s / 1e12 / fp8_peak,
         "stages_ms": stage_ms,
         "roofline": {"bound": "tensor", "kernel": "grouped_gemm_kernel<fp8, swiglu> (GEMM 1)",
                      "achieved": gemm1_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
                      "frac": gemm1_tflops / fp8_peak, "traffic": traffic,
-                     "peak_source": f"{src} bf16 sustained x {FP8_OVER_BF16} (nominal FP8/BF16 ratio)",
+                     "peak_source": f"{src} {peak_kind} x {FP8_OVER_BF16} (nominal FP8/BF16 ratio); timed region "
+                                    f"{elapsed_ms / 1000.0:.2f} s",
                      "flop_per_launch": g1},
         "e2e": {"value": sh.T * e_steps * ws / (e2e_ms / 1000.0), "unit": "tokens/s",
                 "h2d_bytes_per_step": sh.T * sh.d * 2, "d2h_bytes_per_step": sh.T * sh.d * 2},
         "clocks": clocks.summary(),
         "gpu_launches": KERNELS_PER_STEP * args.steps,
     }
+    cpu_rows = []
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         inputs = (u_bufs[0].cpu(), cent.cpu(), bias.cpu(),
                   lambda e: tuple(w.cpu() for w in S.expert_weights(sh, e, device=dev)))
-        n = max(1, int(os.environ.get("CPU_BASELINE_TOKENS", "12")))
+        n = max(1, int(os.environ.get("CPU_BASELINE_TOKENS", str(ORACLE_TOKENS))))
         v, dt, cores = oracle_sample_timing(sh, inputs, n, seed=99)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{n} tokens of the same workload ({dt:.1f} s): routing, FP8 "
                                           f"quantisation of the tokens and of their experts' weights, FFNs, combine"}
+    if rank == 0 and not args.no_configs:
+        # the benchmark's other workloads, each alone, L2 flushed before every launch
+        flush = L2Flush(dev)
+        cb = ws == 1 and not args.no_cpu_baseline
+        line["configs"] = {
+            "tiny_bf16_layer": case_tiny(moe, S, dev, args, flush, cpu_baseline=cb),
+            "route_dispatch_t16384": case_route(moe, S, dev, args, flush, cpu_baseline=cb),
+            "fp8_gemm_4096x4096x7168": case_gemm(moe, S, dev, args, flush, cpu_baseline=cb),
+        }
+        for dsh in S.DECODE_V3:
+            line["configs"][f"decode_t{dsh.T}"] = case_decode(moe, S, dev, args, flush, layer, dsh,
+                                                              cpu_baseline=cb)
+        assert moe.device_status() == 0
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -344,7 +387,7 @@ def run_ours(args):
 
 
 # --------------------------------------------------------------------------
-# single-kernel workloads (the other configurations, and small profiling cases)
+# single workloads: the benchmark's other configurations (each timed alone)
 # --------------------------------------------------------------------------
 
 class L2Flush:
@@ -379,6 +422,176 @@ def time_launches(fn, steps, warmup, flush=None):
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
+def _cpu(value, unit, cores, sample):
+    return {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+
+
+def case_tiny(moe, S, dev, args, flush, cpu_baseline=True):
+    """The tiny bf16 layer (T=128, d=256, 16 routed + 1 shared, top-4, I=128,
+    b=0): launch-latency bound; reported as microseconds per layer call."""
+    import numpy as np
+    import torch
+
+    import oracle
+    sh = S.TINY
+    cent = S.centroids(sh).to(dev)
+    bias = S.bias(sh, zero=True).to(dev)
+    layer = moe.MoELayer.build(sh.d, sh.N, sh.K, sh.I, cent, bias, lambda e: S.expert_weights(sh, e, device=dev),
+                               fp8=False, gamma=sh.gamma)
+    u = S.tokens(sh, device=dev)
+    out = torch.empty_like(u)
+    ms = time_launches(lambda: layer.forward(u, out, update_bias=False), args.steps, args.warmup, flush)
+    R = sh.T * sh.K + sh.T
+    flop = 2.0 * R * 3 * sh.I * sh.d + 2.0 * sh.T * sh.N * sh.d
+    pk, src = peaks()
+    res = {"workload": "tiny-bf16-layer T=128 d=256 16+1 experts top-4 I=128", "ms": ms, "us_per_layer": 1e3 * ms,
+           "tokens_per_s": sh.T / ms * 1e3, "dtype": "bf16", "launches": KERNELS_PER_STEP + 1,
+           "roofline": {"bound": "tensor", "achieved": flop / ms / 1e9, "peak": pk["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": flop / ms / 1e9 / pk["bf16_tflops"], "traffic": None,
+                        "note": "launch-latency bound: 11 launches of a few microseconds each",
+                        "peak_source": f"{src} bf16 burst"}}
+    if cpu_baseline:
+        w = {e: S.expert_weights(sh, e) for e in range(sh.N + 1)}
+        t0 = time.perf_counter()
+        oracle.layer_tokens(u.cpu(), cent.cpu(), bias.cpu(), sh.K, lambda e: w[e], np.arange(sh.T), fp8=False)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = _cpu(sh.T / dt, "tokens/s", oracle.threads(), f"the whole layer, all {sh.T} tokens "
+                                   f"({dt:.2f} s)")
+    del layer
+    return res
+
+
+def case_route(moe, S, dev, args, flush, cpu_baseline=True):
+    """Routing + dispatch at T=16384, d=7168, 256 fp32 centroids, top-8: gate
+    logits, affinities, biased top-8, gates, loads (routing from centroids
+    prepared once), the stable counting sort and scatter of bf16 rows, and the
+    bias update. HBM bound."""
+    import numpy as np
+
+    import oracle
+    sh = S.ROUTE_V3
+    T, d, N, K = sh.T, sh.d, sh.N, sh.K
+    u = S.tokens(sh, device=dev)
+    cent = S.centroids(sh, device=dev)
+    bias = S.bias(sh, device=dev)
+    L = moe.load_library()
+    prepared = moe.moe_route_prepare_centroids(cent)
+    ws_r = moe._ws(L.moe_route_prepared_workspace_size(T, d, N, moe.MOE_DTYPE_F32), dev)
+    ws_p = moe._ws(L.moe_permute_workspace_size(T, N), dev)
+    idx, gates, loads, _ = moe.moe_route_prepared(u, prepared, moe.MOE_DTYPE_F32, N, bias, K, workspace=ws_r)
+    moe.moe_permute(u, idx, N, workspace=ws_p)
+
+    def step():
+        moe.moe_route_prepared(u, prepared, moe.MOE_DTYPE_F32, N, bias, K, workspace=ws_r)
+        moe.moe_permute(u, idx, N, workspace=ws_p)
+        moe.moe_bias_update(bias, loads, T, K, sh.gamma)
+    ms = time_launches(step, args.steps, args.warmup, flush)
+    ms_route = time_launches(lambda: moe.moe_route_prepared(u, prepared, moe.MOE_DTYPE_F32, N, bias, K,
+                                                            workspace=ws_r), args.steps, args.warmup, flush)
+    ms_perm = time_launches(lambda: moe.moe_permute(u, idx, N, workspace=ws_p), args.steps, args.warmup, flush)
+    # algorithmic bytes: u read twice (gate, scatter), the prepared centroids, the K bf16 copies
+    # written, indices / gates / rows / tokens (int32 or fp32) written, bias and loads
+    alg = 2 * T * d * 2 + N * 3 * d * 2 + T * K * d * 2 + T * K * 4 * 4 + N * 12
+    pk, src = peaks()
+    res = {"workload": "route-dispatch-16384x7168-256e-top8", "ms": ms, "tokens_per_s": T / ms * 1e3,
+           "ms_route": ms_route, "ms_permute": ms_perm,
+           "permute_gbs": (T * d * 2 + T * K * d * 2 + T * K * 12) / ms_perm / 1e6,
+           "roofline": {"bound": "hbm", "achieved": alg / ms / 1e6, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": alg / ms / 1e6 / pk["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
+                        "peak_source": f"{src} hbm copy"},
+           "l2": "flushed before each step"}
+    if cpu_baseline:
+        n = 512
+        uc, ec, bc = u[:n].cpu(), cent.cpu(), bias.cpu()
+        t0 = time.perf_counter()
+        r = oracle.route(uc, ec, bc, K)
+        oracle.permute(r.topk_idx, N)
+        oracle.bias_update(bc.numpy(), r.loads, n, K, sh.gamma)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = _cpu(n / dt, "tokens/s", oracle.threads(),
+                                   f"routing, permutation indices and bias update of {n} of the {T} tokens "
+                                   f"({dt:.2f} s)")
+    return res
+
+
+def case_gemm(moe, S, dev, args, flush, cpu_baseline=True):
+    """The dense FP8 block-scaled GEMM: A 4096x7168 (1x128 scales, 0.1% outliers
+    x100), B 4096x7168 (128x128 scales), bf16 out; tensor bound."""
+    import torch
+
+    import oracle
+    cfg = S.GEMM_V3
+    a, b = S.gemm_operands(cfg["M"], cfg["K"], cfg["N"], device=dev)
+    qa, sa = moe.fp8_quant_1x128(a)
+    qb, sb = moe.fp8_quant_128x128(b)
+    qb3, sb3 = qb[None], sb[None]
+    offs = torch.tensor([0, cfg["M"]], dtype=torch.int32, device=dev)
+    C = moe.fp8_grouped_gemm(qa, sa, qb3, sb3, offs, moe.MOE_EPI_BF16)
+    ms = time_launches(lambda: moe.fp8_grouped_gemm(qa, sa, qb3, sb3, offs, moe.MOE_EPI_BF16, C=C),
+                       args.steps, args.warmup, flush)
+    flop = 2.0 * cfg["M"] * cfg["N"] * cfg["K"]
+    pk, src = peaks()
+    peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    res = {"workload": "fp8-gemm-4096x4096x7168", "ms": ms, "tflops": flop / ms / 1e9,
+           "roofline": {"bound": "tensor", "achieved": flop / ms / 1e9, "peak": peak, "unit": "TFLOP/s",
+                        "frac": flop / ms / 1e9 / peak, "traffic": None,
+                        "peak_source": f"{src} bf16 burst x {FP8_OVER_BF16}"},
+           "l2": "flushed before each launch"}
+    if cpu_baseline:
+        rows = 16
+        qa_o, sa_o = oracle.quant_1x128(a[:rows].cpu())
+        qb_o, sb_o = oracle.quant_128x128(b.cpu())
+        t0 = time.perf_counter()
+        oracle.fp8_gemm(qa_o, sa_o, qb_o, sb_o)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = _cpu(2.0 * rows * cfg["N"] * cfg["K"] / dt / 1e12, "TFLOP/s", oracle.threads(),
+                                   f"{rows} of the {cfg['M']} output rows from operands the oracle quantised "
+                                   f"itself ({dt:.2f} s)")
+    return res
+
+
+def case_decode(moe, S, dev, args, flush, v3_layer, dsh, cpu_baseline=True):
+    """A group-limited decode batch (T=64 or 256; 8 groups of 32 experts, top-4
+    groups, top-8 within) through the V3 layer's resident FP8 weights; bound by
+    streaming the active experts' weights from HBM."""
+    import torch
+
+    import oracle
+    layer = moe.MoELayer(dsh.d, dsh.N, dsh.K, dsh.I, v3_layer.centroids, v3_layer.bias.clone(), v3_layer.w13,
+                         v3_layer.w2, v3_layer.w13_scales, v3_layer.w2_scales, n_groups=dsh.n_groups,
+                         topk_groups=dsh.topk_groups, gamma=dsh.gamma)
+    u = S.tokens(dsh, seed=3, device=dev)
+    out = torch.empty_like(u)
+    ms = time_launches(lambda: layer.forward(u, out, update_bias=False), args.steps, args.warmup, flush)
+    active = int((layer.loads > 0).sum().item()) + 1
+    per_expert = 3 * dsh.I * dsh.d + 4 * (3 * dsh.I * dsh.d // 16384)
+    alg = active * per_expert + 2 * dsh.T * dsh.d * 2
+    pk, src = peaks()
+    res = {"workload": dsh.name, "ms": ms, "tokens_per_s": dsh.T / ms * 1e3, "active_experts": active,
+           "roofline": {"bound": "hbm", "achieved": alg / ms / 1e6, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": alg / ms / 1e6 / pk["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
+                        "peak_source": f"{src} hbm copy"},
+           "l2": "flushed before each step"}
+    if cpu_baseline:
+        import numpy as np
+        n = 2
+        inputs = (u.cpu(), v3_layer.centroids.cpu(), v3_layer.bias.cpu(),
+                  lambda e: tuple(w.cpu() for w in S.expert_weights(dsh, e, device=dev)))
+        toks = np.arange(n)
+        r = oracle.route(inputs[0][torch.as_tensor(toks)], inputs[1], inputs[2], dsh.K, dsh.n_groups,
+                         dsh.topk_groups)
+        cache = {e: inputs[3](e) for e in sorted(set(r.topk_idx.ravel().tolist()) | {dsh.N})}
+        t0 = time.perf_counter()
+        oracle.layer_tokens(inputs[0], inputs[1], inputs[2], dsh.K, lambda e: cache[e], toks, fp8=True,
+                            n_groups=dsh.n_groups, topk_groups=dsh.topk_groups)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = _cpu(n / dt, "tokens/s", oracle.threads(),
+                                   f"{n} tokens: group-limited routing, FP8 quantisation of the tokens and of "
+                                   f"their experts' weights, FFNs, combine ({dt:.1f} s)")
+    del layer
+    return res
+
+
 def grouped_fp8_operands(moe, S, dev, rows_per_group, G, Nd, Kd, seed=0):
     """Row-grouped E4M3 activations [G*rows, Kd] and G weight matrices [Nd, Kd],
     drawn N(0,1) and N(0, 1/sqrt(Kd)) and quantised by this library's kernels."""
@@ -396,6 +609,26 @@ def grouped_fp8_operands(moe, S, dev, rows_per_group, G, Nd, Kd, seed=0):
     return qa, sa, qb, sb, offs
 
 
+def case_gemm_slice(moe, S, dev, args, flush, which):
+    """One expert's average share of the V3 layer's GEMMs: 33 groups (32 routed +
+    shared) of 256 rows; GEMM 1 (SwiGLU + FP8 out) or GEMM 2 (bf16 out). A small
+    case for profiling the grouped GEMM."""
+    G, rows = 33, 256
+    Nd, Kd, epi = (4096, 7168, moe.MOE_EPI_SWIGLU_FP8) if which == 1 else (7168, 2048, moe.MOE_EPI_BF16)
+    qa, sa, qb, sb, offs = grouped_fp8_operands(moe, S, dev, rows, G, Nd, Kd)
+    M = G * rows
+    outs = moe.fp8_grouped_gemm(qa, sa, qb, sb, offs, epi)
+    C, cs = outs if epi == moe.MOE_EPI_SWIGLU_FP8 else (outs, None)
+    ms = time_launches(lambda: moe.fp8_grouped_gemm(qa, sa, qb, sb, offs, epi, C=C, c_scales=cs),
+                       args.steps, args.warmup, flush)
+    flop = 2.0 * M * Nd * Kd
+    pk, src = peaks()
+    peak = pk["bf16_tflops"] * FP8_OVER_BF16
+    return {"workload": f"grouped-fp8-{G}x{rows}x{Nd}x{Kd}", "ms": ms, "tflops": flop / ms / 1e9,
+            "frac_of_fp8_peak": flop / ms / 1e9 / peak, "peak_source": f"{src} bf16 burst x {FP8_OVER_BF16}",
+            "l2": "flushed before each launch"}
+
+
 def run_case(args):
     import torch
 
@@ -403,81 +636,26 @@ def run_case(args):
     import synthetic as S
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    pk, src = peaks()
     flush = L2Flush(dev)
     line = {"case": args.case, "steps": args.steps, "warmup": args.warmup, "data": "synthetic"}
-    if args.case in ("gemm", "gemm1-small", "gemm2-small"):
-        if args.case == "gemm":
-            cfg = S.GEMM_V3
-            a, b = S.gemm_operands(cfg["M"], cfg["K"], cfg["N"], device=dev)
-            qa, sa = moe.fp8_quant_1x128(a)
-            qb, sb = moe.fp8_quant_128x128(b)
-            qb, sb = qb[None], sb[None]
-            offs = torch.tensor([0, cfg["M"]], dtype=torch.int32, device=dev)
-            M, Nd, Kd, epi = cfg["M"], cfg["N"], cfg["K"], moe.MOE_EPI_BF16
-            workload = "fp8-gemm-4096x4096x7168"
-        else:
-            # one expert's average share of the V3 layer: 33 groups (32 routed + shared) of 256 rows
-            G, rows = 33, 256
-            Nd, Kd, epi = (4096, 7168, moe.MOE_EPI_SWIGLU_FP8) if args.case == "gemm1-small" else \
-                          (7168, 2048, moe.MOE_EPI_BF16)
-            qa, sa, qb, sb, offs = grouped_fp8_operands(moe, S, dev, rows, G, Nd, Kd)
-            M = G * rows
-            workload = f"grouped-fp8-{G}x{rows}x{Nd}x{Kd}"
-        outs = moe.fp8_grouped_gemm(qa, sa, qb, sb, offs, epi)
-        C, cs = outs if epi == moe.MOE_EPI_SWIGLU_FP8 else (outs, None)
-        ms = time_launches(lambda: moe.fp8_grouped_gemm(qa, sa, qb, sb, offs, epi, C=C, c_scales=cs),
-                           args.steps, args.warmup, flush)
-        assert moe.device_status() == 0
-        flop = 2.0 * M * Nd * Kd
-        fp8_peak = pk["bf16_tflops"] * FP8_OVER_BF16
-        line.update(workload=workload, ms=ms, tflops=flop / ms / 1e9,
-                    frac_of_fp8_peak=flop / ms / 1e9 / fp8_peak,
-                    peak_source=f"{src} bf16 burst x {FP8_OVER_BF16}", l2="flushed before each launch")
+    cb = not args.no_cpu_baseline
+    if args.case == "gemm":
+        line.update(case_gemm(moe, S, dev, args, flush, cpu_baseline=cb))
+    elif args.case in ("gemm1-small", "gemm2-small"):
+        line.update(case_gemm_slice(moe, S, dev, args, flush, 1 if args.case == "gemm1-small" else 2))
     elif args.case == "route":
-        sh = S.ROUTE_V3
-        u = S.tokens(sh, device=dev)
-        cent = S.centroids(sh, device=dev)
-        bias = S.bias(sh, device=dev)
-        T, d, N, K = sh.T, sh.d, sh.N, sh.K
-        L = moe.load_library()
-        ws_r = moe._ws(L.moe_route_workspace_size(T, d, N, moe.MOE_DTYPE_F32), dev)
-        ws_p = moe._ws(L.moe_permute_workspace_size(T, N), dev)
-        idx, gates, loads, _ = moe.moe_route(u, cent, bias, K, workspace=ws_r)
-        off, perm, dest, xp, _ = moe.moe_permute(u, idx, N, workspace=ws_p)
-
-        def step():
-            moe.moe_route(u, cent, bias, K, workspace=ws_r)
-            moe.moe_permute(u, idx, N, workspace=ws_p)
-            moe.moe_bias_update(bias, loads, T, K, sh.gamma)
-        ms = time_launches(step, args.steps, args.warmup, flush)
-        ms_route = time_launches(lambda: moe.moe_route(u, cent, bias, K, workspace=ws_r), args.steps,
-                                 args.warmup, flush)
-        ms_perm = time_launches(lambda: moe.moe_permute(u, idx, N, workspace=ws_p), args.steps, args.warmup, flush)
-        assert moe.device_status() == 0
-        # algorithmic bytes: u read twice (gate, scatter), centroids, bias, the K bf16 copies written,
-        # indices / gates / rows / tokens (int32 or fp32) written
-        alg = 2 * T * d * 2 + N * d * 4 + T * K * d * 2 + T * K * 4 * 4 + N * 12
-        line.update(workload="route-dispatch-16384x7168-256e-top8", ms=ms, tokens_per_s=T / ms * 1e3,
-                    gbs=alg / ms / 1e6, frac_of_hbm=alg / ms / 1e6 / pk["hbm_gbs"], ms_route=ms_route,
-                    ms_permute=ms_perm, permute_gbs=(T * d * 2 + T * K * d * 2 + T * K * 12) / ms_perm / 1e6,
-                    algorithmic_bytes=alg, l2="flushed before each step")
+        line.update(case_route(moe, S, dev, args, flush, cpu_baseline=cb))
+    elif args.case == "tiny":
+        line.update(case_tiny(moe, S, dev, args, flush, cpu_baseline=cb))
     elif args.case in ("decode64", "decode256"):
-        sh = S.DECODE_V3[0 if args.case == "decode64" else 1]
+        sh = S.LAYER_V3
         cent = S.centroids(sh, zipf=True).to(dev)
         bias = S.bias(sh).to(dev)
-        layer = moe.MoELayer.build(sh.d, sh.N, sh.K, sh.I, cent, bias,
-                                   lambda e: S.expert_weights(sh, e, device=dev), fp8=True, gamma=sh.gamma,
-                                   n_groups=sh.n_groups, topk_groups=sh.topk_groups)
-        u = S.tokens(sh, seed=3, device=dev)
-        out = torch.empty_like(u)
-        ms = time_launches(lambda: layer.forward(u, out, update_bias=False), args.steps, args.warmup, flush)
-        assert moe.device_status() == 0
-        active = int((layer.loads > 0).sum().item()) + 1
-        per_expert = 3 * sh.I * sh.d + 4 * (3 * sh.I * sh.d // 16384)
-        alg = active * per_expert + 2 * sh.T * sh.d * 2
-        line.update(workload=sh.name, ms=ms, tokens_per_s=sh.T / ms * 1e3, active_experts=active,
-                    gbs=alg / ms / 1e6, frac_of_hbm=alg / ms / 1e6 / pk["hbm_gbs"], l2="flushed before each step")
+        v3 = moe.MoELayer.build(sh.d, sh.N, sh.K, sh.I, cent, bias, lambda e: S.expert_weights(sh, e, device=dev),
+                                fp8=True, gamma=sh.gamma)
+        dsh = S.DECODE_V3[0 if args.case == "decode64" else 1]
+        line.update(case_decode(moe, S, dev, args, flush, v3, dsh, cpu_baseline=cb))
+    assert moe.device_status() == 0
     print(json.dumps(line), flush=True)
 
 
@@ -488,9 +666,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="time the V3 layer only")
     ap.add_argument("--case", default="layer",
-                    choices=["layer", "gemm", "gemm1-small", "gemm2-small", "route", "decode64", "decode256"],
-                    help="layer: the V3 layer step (the benchmark line); the others time one workload alone")
+                    choices=["layer", "tiny", "route", "gemm", "gemm1-small", "gemm2-small", "decode64",
+                             "decode256"],
+                    help="layer: the V3 layer step with every other workload (the benchmark line); the others "
+                         "time one workload alone")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

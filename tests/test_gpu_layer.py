@@ -39,7 +39,10 @@ def _cpu_weights(sh):
     return lambda e: tuple(w.cpu() for w in S.expert_weights(sh, e, device="cuda"))
 
 
-def _run_and_check(sh, tokens=None, zipf=False, zero_bias=False, u_seed=0):
+def _run_and_check(sh, tokens=None, zipf=False, zero_bias=False, u_seed=0, pick=None):
+    """Runs the layer on the GPU, then checks routing, loads and the bias for all
+    tokens and h' for `tokens` (all if None), or for pick(topk_idx, loads) when
+    the tokens to check depend on the routing."""
     m = _lib()
     layer = _build(sh, zipf=zipf, zero_bias=zero_bias)
     b0 = layer.bias.cpu().numpy().copy()
@@ -50,6 +53,8 @@ def _run_and_check(sh, tokens=None, zipf=False, zero_bias=False, u_seed=0):
     out = layer.forward(u.cuda(), topk_idx=idx, gates=gates, update_bias=True)
     assert m.device_status() == 0
     idx_g, loads_g = idx.cpu().numpy(), layer.loads.cpu().numpy()
+    if pick is not None:
+        tokens = pick(idx_g, loads_g)
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     ref, r, _ = oracle.layer_tokens(u, layer.centroids.cpu(), torch.from_numpy(b0), sh.K, _cpu_weights(sh), tokens,
                                     fp8=sh.fp8, n_groups=sh.n_groups, topk_groups=sh.topk_groups, delta=DELTA)
@@ -133,3 +138,17 @@ def test_layer_pipelined_host_calls_match_device_path():
         done[i].synchronize()
         assert torch.equal(out_h[i].view(torch.int16), expect[i].view(torch.int16)), i
     assert _lib().device_status() == 0
+
+
+def test_layer_with_and_without_prepared_centroids_agree():
+    """The layer routes from centroids prepared once at set-up; routing from the
+    raw centroids inside the call gives the same bits."""
+    sh = S.LayerShape(T=130, d=512, N=32, K=4, I=256, name="prepared")
+    layer = _build(sh)
+    u = S.tokens(sh).cuda()
+    a = layer.forward(u, update_bias=False)
+    layer._desc.centroids_prepared = None
+    layer._ws.clear()
+    b = layer.forward(u, update_bias=False)
+    assert _lib().device_status() == 0
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

@@ -1,9 +1,10 @@
 """Full V3-shape layers on the GPU, checked on sampled tokens by the oracle.
 
   * the FP8 layer: T=8192, d=7168, 256 routed + 1 shared experts, I=2048,
-    top-8, Zipf-skewed expert popularity; the oracle checks 256 sampled tokens
-    (seeded uniform, plus the first tokens routed to the hottest and to the
-    coldest used expert) and the routing of all tokens;
+    top-8, Zipf-skewed expert popularity; the oracle checks h' of 256 tokens
+    (the first and last tokens routed to the hottest and to the coldest used
+    expert, whose last rows sit in ragged tail tiles, plus seeded uniform
+    tokens) and the routing, loads and bias update of all tokens;
   * the decode shapes T=64 and T=256 with group-limited routing (8 groups of
     32, top-4 groups by the sum of each group's two best biased affinities).
 """
@@ -22,10 +23,31 @@ def _sample(T, n, seed=5):
     return np.sort(rng.choice(T, n, replace=False))
 
 
+def pick_256(idx, loads, n=256, seed=5):
+    """256 tokens to check: the first and last token routed to the hottest expert
+    and to the coldest expert with any load (the last rows of those groups sit in
+    their last, ragged, 128-row tile; the coldest group is one ragged tile), then
+    seeded uniform tokens up to n."""
+    T = idx.shape[0]
+    hot = int(np.argmax(loads))
+    used = np.nonzero(loads)[0]
+    cold = int(used[np.argmin(loads[used])])
+    forced = []
+    for e in (hot, cold):
+        rows = np.nonzero((idx == e).any(axis=1))[0]
+        forced += [int(rows[0]), int(rows[-1])]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rest = [t for t in rng.permutation(T) if t not in forced][: n - len(set(forced))]
+    toks = np.unique(np.concatenate([forced, rest]).astype(np.int64))
+    assert toks.size == n
+    print(f"V3 layer: hottest expert {hot} ({loads[hot]} rows, {loads[hot] % 128} in its last tile), coldest used "
+          f"expert {cold} ({loads[cold]} rows); checked tokens include {sorted(set(forced))}")
+    return toks
+
+
 def test_layer_v3_fp8_sampled_tokens():
     sh = S.LAYER_V3
-    toks = _sample(sh.T, 254)
-    tau, n_diff = _run_and_check(sh, tokens=toks, zipf=True)
+    tau, n_diff = _run_and_check(sh, zipf=True, pick=pick_256)
     print(f"V3 layer: achieved tau {tau:.3e}, {n_diff} near-tie tokens routed differently")
 
 

@@ -363,8 +363,52 @@ def test_permute_full_size_bf16():
     np.testing.assert_array_equal(off.cpu().numpy(), off_o)
     np.testing.assert_array_equal(perm.cpu().numpy(), perm_o)
     np.testing.assert_array_equal(dest.cpu().numpy(), dest_o)
-    rows = torch.arange(0, T * K, 97, device="cuda")
-    assert torch.equal(xp[rows].view(torch.int16), x[torch.as_tensor(perm_o).cuda()[rows]].view(torch.int16))
+    _assert_rows_equal(xp, x, perm_o)
+
+
+def _assert_rows_equal(xp, x, src, chunk=8192):
+    """Every permuted row equals its source row, byte for byte (compared on the
+    device, `chunk` rows at a time)."""
+    src = torch.as_tensor(src).cuda().long()
+    assert xp.shape[0] == src.numel()
+    for r0 in range(0, src.numel(), chunk):
+        r1 = min(src.numel(), r0 + chunk)
+        assert torch.equal(xp[r0:r1].view(torch.int16), x[src[r0:r1]].view(torch.int16)), f"rows {r0}..{r1}"
+
+
+def test_route_dispatch_full_size_composition():
+    """The route + dispatch workload end to end at T=16384, d=7168, 256 fp32
+    centroids, top-8: moe_route's own output feeds moe_permute (bf16 rows) and
+    moe_bias_update. Routing is checked against the oracle with the certified-gap
+    rule; the permutation (offsets, perm_token, dest_row, every row's bytes) and
+    the updated bias are checked bit-exactly against the oracle run on the GPU's
+    selection."""
+    m = lib()
+    sh = S.ROUTE_V3
+    T, d, N, K = sh.T, sh.d, sh.N, sh.K
+    u, e, b = S.tokens(sh), S.centroids(sh), S.bias(sh)
+    x = cuda(u)
+    idx_t, gates, loads_t, _ = m.moe_route(x, cuda(e), cuda(b), K)
+    off, perm, dest, xp, _ = m.moe_permute(x, idx_t, N)
+    bias_t = cuda(b.clone())
+    m.moe_bias_update(bias_t, loads_t, T, K, sh.gamma)
+    status_ok()
+    idx, loads = idx_t.cpu().numpy(), loads_t.cpu().numpy()
+    r = oracle.route(u, e, b, K, delta=ROUTE_DELTA)
+    same = np.all(idx == r.topk_idx, axis=1)
+    assert np.all(same | r.near_tie), "a token with a certified gap was routed differently"
+    np.testing.assert_array_equal(loads, np.bincount(idx.ravel(), minlength=N))
+    if same.all():
+        np.testing.assert_array_equal(loads, r.loads)
+    np.testing.assert_allclose(gates.cpu().numpy()[same], r.gates[same], rtol=2e-6, atol=0)
+    off_o, perm_o, dest_o = oracle.permute(idx, N)
+    np.testing.assert_array_equal(off.cpu().numpy(), off_o)
+    np.testing.assert_array_equal(perm.cpu().numpy(), perm_o)
+    np.testing.assert_array_equal(dest.cpu().numpy(), dest_o)
+    _assert_rows_equal(xp, x, perm_o)
+    np.testing.assert_array_equal(bias_t.cpu().numpy(), oracle.bias_update(b.numpy(), loads, T, K, sh.gamma))
+    print(f"route+dispatch full size: {int(r.near_tie.sum())} near-tie tokens, {int((~same).sum())} routed "
+          f"differently; loads max {loads.max()}, min {loads.min()}")
 
 
 # --------------------------------------------------------------------------
