@@ -75,6 +75,7 @@ def lib():
                 "oracle_swiglu_quant": (None, [vp, vp, i64, i64, vp, vp, vp, vp]),
                 "oracle_combine": (None, [vp, vp, vp, vp, vp, i64, i64, i32, vp]),
                 "oracle_bias_update": (None, [vp, vp, i32, i64, i32, flt]),
+                "oracle_seq_balance": (None, [vp, vp, i64, i32, i32, i64, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -226,6 +227,21 @@ def bias_update(bias: np.ndarray, loads: np.ndarray, T: int, K: int, gamma: floa
     ld = _c(loads, np.int32)
     lib().oracle_bias_update(_ptr(b), _ptr(ld), b.size, T, K, float(np.float32(gamma)))
     return b
+
+
+def seq_balance(scores: np.ndarray, topk_idx: np.ndarray, K: int, seq_len: int):
+    """Sequence-wise balance statistics (see moe_oracle.c): per sequence of
+    seq_len consecutive tokens (the last may be shorter), the loads [S, N], the
+    mean normalised affinities P [S, N] and sum_i f_i P_i [S]."""
+    sc = _c(scores, np.float64)
+    idx = _c(topk_idx, np.int32)
+    T, N = sc.shape
+    S = (T + seq_len - 1) // seq_len
+    loads = np.empty((S, N), np.int32)
+    prob = np.empty((S, N), np.float64)
+    stat = np.empty(S, np.float64)
+    lib().oracle_seq_balance(_ptr(sc), _ptr(idx), T, N, K, seq_len, _ptr(loads), _ptr(prob), _ptr(stat))
+    return loads, prob, stat
 
 
 # --------------------------------------------------------------------------

@@ -25,6 +25,9 @@
  *             an expert is chosen if s_it + b_i is among the top 8; the bias
  *             affects only the choice, not g.
  *   [nodrop]  same page, "The idea", load-balancing item: no token is dropped.
+ *   [seqloss] learn.ifs.name, bias paragraph: beside the bias, only a tiny
+ *             sequence-wise balancing loss remains, against extreme
+ *             imbalance inside one sequence.
  *
  * Readings where the pages are silent (all listed in the design notes):
  *   affinity s = 1/(1+exp(-u.e_i)); gates g = s/sum(s chosen) with factor 1;
@@ -32,7 +35,11 @@
  *   nearest even, saturating at 448; tile scale = amax/448 as an fp32
  *   division (1 for an all-zero tile) and q = e4m3(x / scale) as an fp32
  *   division; expert FFN = W2 (silu(W1 x) * W3 x); "overloaded" means a load
- *   above the mean T*K/N, "underloaded" below it.
+ *   above the mean T*K/N, "underloaded" below it. The sequence-wise
+ *   balance statistic of a sequence of T_s tokens is sum_i f_i * P_i with
+ *   f_i = N * (pairs routed to i) / (K * T_s) and P_i the mean over the
+ *   sequence of s_i / sum_j s_j (affinities normalised over all N experts);
+ *   the loss weight is the caller's.
  *
  * Every floating-point sum below runs in FP64, in index order.
  */
@@ -516,5 +523,43 @@ void oracle_bias_update(float* bias, const int32_t* loads, int N, int64_t T, int
         int64_t lhs = (int64_t)loads[i] * N;
         if (lhs > mean_num) bias[i] = bias[i] - gamma;
         else if (lhs < mean_num) bias[i] = bias[i] + gamma;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sequence-wise balance statistics [seqloss]                               */
+/* ------------------------------------------------------------------------ */
+
+/* Sequences are the consecutive token ranges [s*seq_len, min(T, (s+1)*seq_len)).
+ * For sequence s of T_s tokens and expert i:
+ *   loads[s][i] = number of (t, k) in the sequence with topk_idx[t,k] == i
+ *   prob[s][i]  = (1/T_s) sum_t scores[t,i] / sum_j scores[t,j]
+ *   stat[s]     = sum_i (N * loads[s][i] / (K * T_s)) * prob[s][i]
+ * scores [T, N] are the affinities s (FP64 here); sums in FP64, in index order. */
+void oracle_seq_balance(const double* scores, const int32_t* topk_idx, int64_t T, int N, int K, int64_t seq_len,
+                        int32_t* loads, double* prob, double* stat)
+{
+    const int64_t S = (T + seq_len - 1) / seq_len;
+    for (int64_t s = 0; s < S; ++s) {
+        const int64_t t0 = s * seq_len, t1 = t0 + seq_len < T ? t0 + seq_len : T;
+        const double Ts = (double)(t1 - t0);
+        int32_t* ld = loads + s * N;
+        double* pr = prob + s * N;
+        for (int i = 0; i < N; ++i) {
+            ld[i] = 0;
+            pr[i] = 0.0;
+        }
+        for (int64_t t = t0; t < t1; ++t) {
+            double row = 0.0;
+            for (int i = 0; i < N; ++i) row += scores[t * N + i];
+            for (int i = 0; i < N; ++i) pr[i] += scores[t * N + i] / row;
+            for (int k = 0; k < K; ++k) ld[topk_idx[t * K + k]] += 1;
+        }
+        double acc = 0.0;
+        for (int i = 0; i < N; ++i) {
+            pr[i] /= Ts;
+            acc += ((double)N * ld[i] / ((double)K * Ts)) * pr[i];
+        }
+        stat[s] = acc;
     }
 }
