@@ -478,6 +478,7 @@ def case_route(moe, S, dev, args, flush, cpu_baseline=True):
     prepared = moe.moe_route_prepare_centroids(cent)
     ws_r = moe._ws(L.moe_route_prepared_workspace_size(T, d, N, moe.MOE_DTYPE_F32), dev)
     ws_p = moe._ws(L.moe_permute_workspace_size(T, N), dev)
+    pk, src = peaks()
     idx, gates, loads, _ = moe.moe_route_prepared(u, prepared, moe.MOE_DTYPE_F32, N, bias, K, workspace=ws_r)
     moe.moe_permute(u, idx, N, workspace=ws_p)
 
@@ -489,13 +490,23 @@ def case_route(moe, S, dev, args, flush, cpu_baseline=True):
     ms_route = time_launches(lambda: moe.moe_route_prepared(u, prepared, moe.MOE_DTYPE_F32, N, bias, K,
                                                             workspace=ws_r), args.steps, args.warmup, flush)
     ms_perm = time_launches(lambda: moe.moe_permute(u, idx, N, workspace=ws_p), args.steps, args.warmup, flush)
+    # sequence-wise balance statistics of the step (sequences of 4096 tokens) from the routing's affinities
+    seq_len = 4096
+    _, _, _, scores = moe.moe_route_prepared(u, prepared, moe.MOE_DTYPE_F32, N, bias, K, want_scores=True,
+                                             workspace=ws_r)
+    ws_b = moe._ws(L.moe_route_balance_stats_workspace_size(T, N, seq_len), dev)
+    ms_bal = time_launches(lambda: moe.moe_route_balance_stats(scores, idx, seq_len, workspace=ws_b), args.steps,
+                           args.warmup, flush)
+    bal_bytes = T * N * 4 + T * K * 4 + (T // seq_len) * N * 8
     # algorithmic bytes: u read twice (gate, scatter), the prepared centroids, the K bf16 copies
     # written, indices / gates / rows / tokens (int32 or fp32) written, bias and loads
     alg = 2 * T * d * 2 + N * 3 * d * 2 + T * K * d * 2 + T * K * 4 * 4 + N * 12
-    pk, src = peaks()
     res = {"workload": "route-dispatch-16384x7168-256e-top8", "ms": ms, "tokens_per_s": T / ms * 1e3,
            "ms_route": ms_route, "ms_permute": ms_perm,
            "permute_gbs": (T * d * 2 + T * K * d * 2 + T * K * 12) / ms_perm / 1e6,
+           "balance_stats": {"seq_len": seq_len, "ms": ms_bal, "gbs": bal_bytes / ms_bal / 1e6,
+                             "frac_of_hbm": bal_bytes / ms_bal / 1e6 / pk["hbm_gbs"],
+                             "note": "reads the [T, N] fp32 affinities once; two launches"},
            "roofline": {"bound": "hbm", "achieved": alg / ms / 1e6, "peak": pk["hbm_gbs"], "unit": "GB/s",
                         "frac": alg / ms / 1e6 / pk["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
                         "peak_source": f"{src} hbm copy"},

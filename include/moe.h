@@ -134,6 +134,25 @@ moe_status moe_route_prepared(const uint16_t* u, int64_t T, int d, const void* p
                               float* scores, void* workspace, size_t workspace_bytes,
                               moe_stream_t stream);
 
+/* Sequence-wise balance statistics of one routing step — learn.ifs.name
+ * summary, bias paragraph: beside the bias, only a tiny sequence-wise
+ * balancing loss remains, against extreme imbalance inside one sequence. The
+ * pages give no formula; the statistic computed here, for each sequence of
+ * seq_len consecutive tokens (the last may be shorter, T_s tokens), is
+ *   seq_loads[s][i] = pairs (t, k) of the sequence with topk_idx[t][k] == i
+ *   seq_prob[s][i]  = (1/T_s) sum_t scores[t][i] / sum_j scores[t][j]
+ *   seq_stat[s]     = sum_i (N seq_loads[s][i] / (K T_s)) seq_prob[s][i]
+ * (the loss weight is the caller's). scores fp32 [T, N]: the affinities s from
+ * moe_route's scores output; topk_idx int32 [T, K] in [0, N). Outputs:
+ * seq_loads int32 [S, N], seq_prob fp32 [S, N], seq_stat fp32 [S], S =
+ * ceil(T / seq_len). Sums run in a fixed order (reproducible bit for bit).
+ * Workspace: moe_route_balance_stats_workspace_size() bytes, 16-byte aligned.
+ * An id outside [0, N) is skipped and sets MOE_ERR_DEVICE_DATA. */
+size_t moe_route_balance_stats_workspace_size(int64_t T, int N, int64_t seq_len);
+moe_status moe_route_balance_stats(const float* scores, const int32_t* topk_idx, int64_t T, int N, int K,
+                                   int64_t seq_len, int32_t* seq_loads, float* seq_prob, float* seq_stat,
+                                   void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Permutation — the single-GPU form of the dispatch step (learn.ifs.name    */
 /* summary, paragraph on all-to-all dispatch/combine): a stable counting     */

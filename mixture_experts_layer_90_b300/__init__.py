@@ -27,6 +27,7 @@ EXPORTS = [
     "moe_route_workspace_size", "moe_route",
     "moe_route_prepared_centroids_size", "moe_route_prepare_centroids",
     "moe_route_prepared_workspace_size", "moe_route_prepared",
+    "moe_route_balance_stats_workspace_size", "moe_route_balance_stats",
     "moe_permute_workspace_size", "moe_permute", "moe_permute_static",
     "fp8_grouped_gemm", "bf16_grouped_gemm",
     "moe_combine", "moe_bias_update", "moe_selftest_wait_timeout",
@@ -86,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_route_prepare_centroids": (i32, [vp, i32, i32, i32, vp, sz, vp]),
         "moe_route_prepared_workspace_size": (sz, [i64, i32, i32, i32]),
         "moe_route_prepared": (i32, [vp, i64, i32, vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]),
+        "moe_route_balance_stats_workspace_size": (sz, [i64, i32, i64]),
+        "moe_route_balance_stats": (i32, [vp, vp, i64, i32, i32, i64, vp, vp, vp, vp, sz, vp]),
         "moe_permute_workspace_size": (sz, [i64, i32]),
         "moe_permute": (i32, [vp, i64, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, sz, vp]),
         "moe_permute_static": (i32, [vp, i64, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]),
@@ -220,6 +223,26 @@ def moe_route_prepared(u, prepared, centroid_dtype, N, bias, K, n_groups=1, topk
                                 _p(idx), _p(gates), _p(loads), _p(scores), _p(ws), ws.numel(), _stream()),
            "moe_route_prepared")
     return idx, gates, loads, scores
+
+
+def moe_route_balance_stats(scores, topk_idx, seq_len, workspace=None):
+    """Sequence-wise balance statistics (include/moe.h) from moe_route's scores
+    [T, N] and topk_idx [T, K] -> (seq_loads int32 [S, N], seq_prob fp32 [S, N],
+    seq_stat fp32 [S]), S = ceil(T / seq_len)."""
+    _require_cuda()
+    L = load_library()
+    T, N = scores.shape
+    K = topk_idx.shape[1]
+    dev = scores.device
+    S = (T + seq_len - 1) // seq_len
+    loads = torch.empty((S, N), dtype=torch.int32, device=dev)
+    prob = torch.empty((S, N), dtype=torch.float32, device=dev)
+    stat = torch.empty((S,), dtype=torch.float32, device=dev)
+    need = L.moe_route_balance_stats_workspace_size(T, N, seq_len)
+    ws = _ws(need, dev) if workspace is None else workspace
+    _check(L.moe_route_balance_stats(_p(scores), _p(topk_idx), T, N, K, seq_len, _p(loads), _p(prob), _p(stat),
+                                     _p(ws), ws.numel(), _stream()), "moe_route_balance_stats")
+    return loads, prob, stat
 
 
 def moe_permute(x, topk_idx, N, out_dtype=MOE_DTYPE_BF16, with_shared=False, workspace=None):

@@ -186,6 +186,28 @@ moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids,
     return MOE_OK;
 }
 
+size_t moe_route_balance_stats_workspace_size(int64_t T, int N, int64_t seq_len) {
+    return moe::balance_ws_bytes(T, N, seq_len);
+}
+
+moe_status moe_route_balance_stats(const float* scores, const int32_t* topk_idx, int64_t T, int N, int K,
+                                   int64_t seq_len, int32_t* seq_loads, float* seq_prob, float* seq_stat,
+                                   void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    REQUIRE(T >= 0 && T <= kMaxRows, "moe_route_balance_stats: T=%lld out of range", (long long)T);
+    REQUIRE(N >= 1 && N <= 1024, "moe_route_balance_stats: N=%d must be in [1, 1024]", N);
+    REQUIRE(K >= 1 && K <= 16 && K <= N, "moe_route_balance_stats: K=%d", K);
+    REQUIRE(seq_len >= 1, "moe_route_balance_stats: seq_len=%lld must be positive", (long long)seq_len);
+    if (T == 0) return MOE_OK;
+    REQUIRE((T + seq_len - 1) / seq_len <= 0x7fffffff, "moe_route_balance_stats: too many sequences");
+    REQUIRE(scores && topk_idx && seq_loads && seq_prob && seq_stat, "moe_route_balance_stats: null pointer");
+    const size_t need = moe::balance_ws_bytes(T, N, seq_len);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return fail(MOE_ERR_WORKSPACE, "moe_route_balance_stats: workspace needs %zu bytes", need);
+    CUDA_OK(moe::launch_balance(scores, topk_idx, T, N, K, seq_len, seq_loads, seq_prob, seq_stat, workspace,
+                                stream));
+    return MOE_OK;
+}
+
 size_t moe_permute_workspace_size(int64_t T, int N) { return moe::permute_ws_bytes(T, N); }
 
 moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K, int out_dtype,

@@ -36,6 +36,11 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
                            int with_shared, int32_t* offsets, int32_t* perm_token, int32_t* dest_row, void* x_perm,
                            float* x_perm_scales, void* ws, cudaStream_t stream);
 
+// Sequence-wise balance statistics (balance.cu).
+size_t balance_ws_bytes(int64_t T, int N, int64_t seq_len);
+cudaError_t launch_balance(const float* scores, const int32_t* topk_idx, int64_t T, int N, int K, int64_t seq_len,
+                           int32_t* seq_loads, float* seq_prob, float* seq_stat, void* ws, cudaStream_t stream);
+
 cudaError_t launch_combine(const uint16_t* u, const uint16_t* y_shared, const uint16_t* y_perm, const float* gates,
                            const int32_t* dest_row, int64_t T, int d, int K, int64_t R, uint16_t* out,
                            cudaStream_t stream);

@@ -2,6 +2,7 @@
 // every kernel live in one module, so one copy of the status word is seen by
 // all kernels and by moe_get_device_status.
 #include "abi.cu"
+#include "balance.cu"
 #include "combine.cu"
 #include "gemm.cu"
 #include "permute.cu"

@@ -181,3 +181,17 @@ def test_prepared_routing_checks_its_arguments(L):
     plain = L.moe_layer_workspace_size(ctypes.byref(w), 8192)
     w.centroids_prepared = 4096
     assert L.moe_layer_workspace_size(ctypes.byref(w), 8192) <= plain - 256 * 3 * 7168 * 2
+
+
+def test_balance_stats_checks_its_arguments(L):
+    p, s = _ok_ptr(), ctypes.c_void_p(0)
+    call = lambda T, N, K, L_, ws_bytes=1 << 20: L.moe_route_balance_stats(  # noqa: E731
+        p, p, T, N, K, L_, p, p, p, p, ws_bytes, s)
+    assert call(100, 2048, 8, 10) == M.MOE_ERR_INVALID_ARG
+    assert call(100, 64, 17, 10) == M.MOE_ERR_INVALID_ARG
+    assert call(100, 4, 8, 10) == M.MOE_ERR_INVALID_ARG        # K > N
+    assert call(100, 64, 8, 0) == M.MOE_ERR_INVALID_ARG
+    need = L.moe_route_balance_stats_workspace_size(1000, 64, 128)
+    assert need >= 8 * 2 * 64 * 8                              # 8 sequences x 2 chunks x 64 experts x 8 bytes
+    assert call(1000, 64, 8, 128, need - 1) == M.MOE_ERR_WORKSPACE
+    assert call(0, 64, 8, 128, 0) == M.MOE_OK                  # no tokens: nothing to do

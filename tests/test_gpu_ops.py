@@ -451,3 +451,75 @@ def test_bias_update_bit_exact(T, K, N):
     bt = cuda(b.copy())
     lib().moe_bias_update(bt, cuda(loads), T, K, 1e-3)
     np.testing.assert_array_equal(bt.cpu().numpy(), oracle.bias_update(b, loads, T, K, 1e-3))
+
+
+# --------------------------------------------------------------------------
+# sequence-wise balance statistics
+# --------------------------------------------------------------------------
+
+def _check_balance(u, e, b, K, seq_len, n_groups=1, topk_groups=1):
+    m = lib()
+    T = u.shape[0]
+    idx, _, _, scores = m.moe_route(cuda(u), cuda(e), cuda(b), K, n_groups, topk_groups, want_scores=True)
+    loads, prob, stat = m.moe_route_balance_stats(scores, idx, seq_len)
+    loads2, prob2, stat2 = m.moe_route_balance_stats(scores, idx, seq_len)
+    status_ok()
+    # fixed summation order: a second call gives the same bits
+    assert torch.equal(loads, loads2) and torch.equal(prob, prob2) and torch.equal(stat, stat2)
+    r = oracle.route(u, e, b, K, n_groups, topk_groups, delta=ROUTE_DELTA, want_scores=True)
+    idx_g = idx.cpu().numpy()
+    same = np.all(idx_g == r.topk_idx, axis=1)
+    assert np.all(same | r.near_tie)
+    ol, op, os_ = oracle.seq_balance(r.scores, r.topk_idx, K, seq_len)
+    if same.all():
+        np.testing.assert_array_equal(loads.cpu().numpy(), ol)
+    else:
+        # near-tie tokens routed to another equally good set: loads follow the GPU's selection
+        np.testing.assert_array_equal(loads.cpu().numpy(), oracle.seq_balance(r.scores, idx_g, K, seq_len)[0])
+    # P from fp32 affinities (|s - s_oracle| <= 5e-6) summed in fp32
+    np.testing.assert_allclose(prob.cpu().numpy(), op, rtol=2e-5, atol=1e-7)
+    gl = loads.cpu().numpy().astype(np.float64)
+    lens = np.array([min(seq_len, T - t0) for t0 in range(0, T, seq_len)], np.float64)
+    ref_stat = ((e.shape[0] * gl / (K * lens[:, None])) * op).sum(axis=1)
+    np.testing.assert_allclose(stat.cpu().numpy(), ref_stat, rtol=2e-5)
+    if same.all():
+        np.testing.assert_allclose(stat.cpu().numpy(), os_, rtol=2e-5)
+    return stat.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,d,N,K,seq_len", [(1000, 512, 64, 6, 128), (77, 256, 16, 4, 1000), (300, 512, 256, 8, 64)])
+def test_balance_stats(T, d, N, K, seq_len):
+    u, e, b = _route_case(T, d, N, f32=True)
+    _check_balance(u, e, b, K, seq_len)
+
+
+def test_balance_stats_group_limited():
+    u, e, b = _route_case(512, 512, 256, f32=True)
+    _check_balance(u, e, b, 8, 200, n_groups=8, topk_groups=4)
+
+
+def test_balance_stats_closed_forms():
+    """Equal affinities give 1 whatever the routing; every token sending its
+    pairs to experts 0..K-1 with all affinity there gives N/K."""
+    m = lib()
+    T, N, K = 256, 32, 4
+    idx = torch.tensor(_rand_topk(T, N, K, seed=7))
+    sc = torch.full((T, N), 0.3)
+    _, prob, stat = m.moe_route_balance_stats(cuda(sc), cuda(idx), 100)
+    status_ok()
+    np.testing.assert_allclose(prob.cpu().numpy(), 1.0 / N, rtol=1e-6)
+    np.testing.assert_allclose(stat.cpu().numpy(), 1.0, rtol=1e-6)
+    idx = torch.arange(K, dtype=torch.int32).repeat(T, 1)
+    sc = torch.zeros((T, N))
+    sc[:, :K] = 0.7
+    loads, _, stat = m.moe_route_balance_stats(cuda(sc), cuda(idx), T)
+    status_ok()
+    assert loads[0, :K].eq(T).all() and loads[0, K:].eq(0).all()
+    np.testing.assert_allclose(stat.cpu().numpy(), N / K, rtol=1e-6)
+
+
+def test_balance_stats_full_size():
+    """The route + dispatch workload (T=16384, 256 experts, top-8) in sequences of 4096 tokens."""
+    sh = S.ROUTE_V3
+    stat = _check_balance(S.tokens(sh), S.centroids(sh), S.bias(sh), sh.K, 4096)
+    print(f"sequence-wise balance statistic per sequence: {stat}")
