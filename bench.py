@@ -603,6 +603,41 @@ def case_decode(moe, S, dev, args, flush, v3_layer, dsh, cpu_baseline=True):
     return res
 
 
+def case_dispatch(moe, S, dev, args, flush, which):
+    """The V3 layer's dispatch (permute with 1x128 E4M3 quantisation and the shared
+    expert's rows, `permute-fp8`) or combine (`combine`) alone, T = 8192, d = 7168,
+    256 experts, top-8, on seeded ids. HBM bound."""
+    import torch
+
+    sh = S.LAYER_V3
+    T, d, N, K = sh.T, sh.d, sh.N, sh.K
+    pk, src = peaks()
+    h = S.bits(S.key(0, "case-topk", T, N, K), 0, T * N).view(T, N)
+    idx = torch.sort(torch.argsort(h, dim=1)[:, :K], dim=1).values.to(torch.int32).to(dev)
+    u = S.tokens(sh, device=dev)
+    L = moe.load_library()
+    ws_p = moe._ws(L.moe_permute_workspace_size(T, N), dev)
+    off, perm, dest, xp, xs = moe.moe_permute(u, idx, N, moe.MOE_DTYPE_E4M3, with_shared=True, workspace=ws_p)
+    R = T * K + T
+    if which == "permute-fp8":
+        fn = lambda: moe.moe_permute(u, idx, N, moe.MOE_DTYPE_E4M3, with_shared=True, workspace=ws_p)  # noqa: E731
+        alg = T * d * 2 + R * (d + d // 128 * 4) + T * K * 4 * 3 + N * 8
+        workload = "permute-fp8-8192x7168-256e-top8+shared"
+    else:
+        y = S.normal((R, d), 0.5, S.key(0, "case-y", R, d), device=dev)
+        g = torch.full((T, K), 1.0 / K, device=dev)
+        out = torch.empty_like(u)
+        fn = lambda: moe.moe_combine(u, y[T * K:], y, g, dest, out=out)  # noqa: E731
+        alg = (K + 2) * T * d * 2 + T * d * 2 + T * K * 8
+        workload = "combine-8192x7168-top8+shared"
+    ms = time_launches(fn, args.steps, args.warmup, flush)
+    return {"workload": workload, "ms": ms, "tokens_per_s": T / ms * 1e3,
+            "roofline": {"bound": "hbm", "achieved": alg / ms / 1e6, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": alg / ms / 1e6 / pk["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
+                         "peak_source": f"{src} hbm copy"},
+            "l2": "flushed before each launch"}
+
+
 def grouped_fp8_operands(moe, S, dev, rows_per_group, G, Nd, Kd, seed=0):
     """Row-grouped E4M3 activations [G*rows, Kd] and G weight matrices [Nd, Kd],
     drawn N(0,1) and N(0, 1/sqrt(Kd)) and quantised by this library's kernels."""
@@ -658,6 +693,8 @@ def run_case(args):
         line.update(case_route(moe, S, dev, args, flush, cpu_baseline=cb))
     elif args.case == "tiny":
         line.update(case_tiny(moe, S, dev, args, flush, cpu_baseline=cb))
+    elif args.case in ("permute-fp8", "combine"):
+        line.update(case_dispatch(moe, S, dev, args, flush, args.case))
     elif args.case in ("decode64", "decode256"):
         sh = S.LAYER_V3
         cent = S.centroids(sh, zipf=True).to(dev)
@@ -680,7 +717,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="time the V3 layer only")
     ap.add_argument("--case", default="layer",
                     choices=["layer", "tiny", "route", "gemm", "gemm1-small", "gemm2-small", "decode64",
-                             "decode256"],
+                             "decode256", "permute-fp8", "combine"],
                     help="layer: the V3 layer step with every other workload (the benchmark line); the others "
                          "time one workload alone")
     args = ap.parse_args()
