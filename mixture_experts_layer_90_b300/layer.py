@@ -118,6 +118,21 @@ class MoELayer:
                "moe_layer_forward")
         return out
 
+    def capture(self, u: torch.Tensor, out: torch.Tensor = None, update_bias: bool = True) -> "LayerGraph":
+        """Records one forward on the static buffers u -> out into a CUDA graph
+        (the library's calls are asynchronous, allocate nothing and never
+        synchronise, so the whole launch sequence can be captured). Replaying it
+        runs the layer on whatever u holds at replay time, writing out, the loads
+        and, with update_bias, the bias. One eager call runs first, outside the
+        capture, so that per-device set-up is done before it."""
+        out = torch.empty_like(u) if out is None else out
+        self.forward(u, out, update_bias=False)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.forward(u, out, update_bias=update_bias)
+        return LayerGraph(g, u, out)
+
     def forward_host(self, u_host: torch.Tensor, out_host: torch.Tensor, update_bias: bool = True):
         """Same with u/h' in (pinned) host memory: copies in and out inside the call."""
         T = u_host.shape[0]
@@ -143,3 +158,14 @@ class MoELayer:
             ctypes.byref(outs), int(update_bias), int(slot), _p(ws), ws.numel(), _stream(),
             ctypes.c_void_p(done.cuda_event)), "moe_layer_forward_host_pipelined")
         return out_host
+
+
+class LayerGraph:
+    """A captured layer forward: copy a batch into `u`, call replay(), read `out`."""
+
+    def __init__(self, graph, u, out):
+        self.graph, self.u, self.out = graph, u, out
+
+    def replay(self) -> torch.Tensor:
+        self.graph.replay()
+        return self.out

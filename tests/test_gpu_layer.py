@@ -152,3 +152,23 @@ def test_layer_with_and_without_prepared_centroids_agree():
     b = layer.forward(u, update_bias=False)
     assert _lib().device_status() == 0
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_layer_graph_replay_matches_eager(fp8):
+    """The layer captured in a CUDA graph and replayed on new batches gives the
+    same bits as the eager call: h', the loads and the bias after two updates."""
+    sh = S.LayerShape(T=128, d=256, N=16, K=4, I=128, fp8=fp8, centroid_f32=fp8, name=f"graph-{fp8}")
+    eager, graphed = _build(sh), _build(sh)
+    u = torch.empty((sh.T, sh.d), dtype=torch.bfloat16, device="cuda")
+    g = graphed.capture(u)
+    for seed in (21, 22):
+        batch = S.tokens(sh, seed=seed).cuda()
+        ref = eager.forward(batch)
+        u.copy_(batch)
+        got = g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(graphed.loads, eager.loads)
+        assert torch.equal(graphed.bias, eager.bias)
+    assert _lib().device_status() == 0
