@@ -124,14 +124,16 @@ class MoELayer:
         synchronise, so the whole launch sequence can be captured). Replaying it
         runs the layer on whatever u holds at replay time, writing out, the loads
         and, with update_bias, the bias. One eager call runs first, outside the
-        capture, so that per-device set-up is done before it."""
+        capture, so that per-device set-up is done before it. The graph uses
+        this layer's weights and its cached workspace for u's row count: the
+        LayerGraph holds the layer, so they outlive it."""
         out = torch.empty_like(u) if out is None else out
         self.forward(u, out, update_bias=False)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.forward(u, out, update_bias=update_bias)
-        return LayerGraph(g, u, out)
+        return LayerGraph(g, u, out, self)
 
     def forward_host(self, u_host: torch.Tensor, out_host: torch.Tensor, update_bias: bool = True):
         """Same with u/h' in (pinned) host memory: copies in and out inside the call."""
@@ -163,8 +165,8 @@ class MoELayer:
 class LayerGraph:
     """A captured layer forward: copy a batch into `u`, call replay(), read `out`."""
 
-    def __init__(self, graph, u, out):
-        self.graph, self.u, self.out = graph, u, out
+    def __init__(self, graph, u, out, layer):
+        self.graph, self.u, self.out, self.layer = graph, u, out, layer
 
     def replay(self) -> torch.Tensor:
         self.graph.replay()
