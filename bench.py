@@ -572,7 +572,8 @@ def case_decode(moe, S, dev, args, flush, v3_layer, dsh, cpu_baseline=True):
     import torch
 
     import oracle
-    layer = moe.MoELayer(dsh.d, dsh.N, dsh.K, dsh.I, v3_layer.centroids, v3_layer.bias.clone(), v3_layer.w13,
+    # the seeded bias, not the V3 layer's after its bench steps: the batch routes the same in every run
+    layer = moe.MoELayer(dsh.d, dsh.N, dsh.K, dsh.I, v3_layer.centroids, S.bias(dsh, device=dev), v3_layer.w13,
                          v3_layer.w2, v3_layer.w13_scales, v3_layer.w2_scales, n_groups=dsh.n_groups,
                          topk_groups=dsh.topk_groups, gamma=dsh.gamma)
     u = S.tokens(dsh, seed=3, device=dev)
@@ -593,7 +594,7 @@ def case_decode(moe, S, dev, args, flush, v3_layer, dsh, cpu_baseline=True):
     if cpu_baseline:
         import numpy as np
         n = 2
-        inputs = (u.cpu(), v3_layer.centroids.cpu(), v3_layer.bias.cpu(),
+        inputs = (u.cpu(), v3_layer.centroids.cpu(), layer.bias.cpu(),
                   lambda e: tuple(w.cpu() for w in S.expert_weights(dsh, e, device=dev)))
         toks = np.arange(n)
         r = oracle.route(inputs[0][torch.as_tensor(toks)], inputs[1], inputs[2], dsh.K, dsh.n_groups,
