@@ -1,4 +1,5 @@
-"""FP64 CPU oracle for the DeepSeekMoE layer forward (test infrastructure).
+"""FP64 CPU oracle for the DeepSeekMoE layer: forward, backward and training
+step (test infrastructure).
 
 Only the tests, the package's smoke check and the benchmark's CPU-baseline
 leg may import this package. It wraps the plain C file `moe_oracle.c`
@@ -11,7 +12,10 @@ tests/test_golden_pages.py against something other than itself (closed forms,
 brute force with numpy, torch's float8_e4m3fn conversion, invariants, the
 figures the pages print). The composed layer is checked against an
 independent brute force on a tiny layer; the pages print no worked example at
-the full V3 shape, so the full-size value rests on those pins.
+the full V3 shape, so the full-size value rests on those pins. The backward
+pass (tests/test_oracle_backward.py) is checked, in its FP64 form, against
+finite differences of an independent forward, and in its FP8 form against
+the FP64 form on block-scaled inputs; the training step as a descent step.
 """
 from __future__ import annotations
 
@@ -76,6 +80,10 @@ def lib():
                 "oracle_combine": (None, [vp, vp, vp, vp, vp, i64, i64, i32, vp]),
                 "oracle_bias_update": (None, [vp, vp, i32, i64, i32, flt]),
                 "oracle_seq_balance": (None, [vp, vp, i64, i32, i32, i64, vp, vp, vp]),
+                "oracle_quant_128x1": (None, [vp, i64, i64, vp, vp]),
+                "oracle_fp8_gemm_kscaled": (None, [vp, vp, vp, vp, i64, i64, i64, vp]),
+                "oracle_quant_128x128_f32": (None, [vp, i64, i64, vp, vp]),
+                "oracle_swiglu_backward": (None, [vp, vp, vp, i64, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -382,3 +390,236 @@ def layer_tokens(u_bf16, centroids, bias, K, expert_weights, tokens, fp8=True, n
             y_tok[rows, ks] = y
     h = bf16_value(u_bits) + y_sh + np.einsum("tk,tkd->td", g, y_tok)
     return h, r, detail
+
+
+# --------------------------------------------------------------------------
+# backward pass and training step (readings in moe_oracle.c, [train])
+# --------------------------------------------------------------------------
+
+def quant_128x1(x: np.ndarray):
+    """(q uint8 [C, Rp], scales fp32 [Rp/128, C]) from fp32 x [R, C]: one scale
+    per (128 consecutive rows, column); Rp = R rounded up to 128, the missing
+    rows counting as zeros; q holds the columns of x as its rows."""
+    x = _c(x, np.float32)
+    R, C = x.shape
+    Rp = (R + 127) // 128 * 128
+    q = np.empty((C, Rp), np.uint8)
+    s = np.empty((Rp // 128, C), np.float32)
+    lib().oracle_quant_128x1(_ptr(x), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def fp8_gemm_kscaled(qa, sa, qb, sb) -> np.ndarray:
+    """FP64 C [M, Nd] = the weight-gradient product of qa [M, Kp] and qb [Nd, Kp]
+    with scales sa [Kp/128, M], sb [Kp/128, Nd] (see moe_oracle.c)."""
+    qa, qb = _c(qa, np.uint8), _c(qb, np.uint8)
+    sa, sb = _c(sa, np.float32), _c(sb, np.float32)
+    M, Kp = qa.shape
+    Nd = qb.shape[0]
+    C = np.empty((M, Nd), np.float64)
+    lib().oracle_fp8_gemm_kscaled(_ptr(qa), _ptr(sa), _ptr(qb), _ptr(sb), M, Nd, Kp, _ptr(C))
+    return C
+
+
+def quant_128x128_f32(w: np.ndarray):
+    """(q uint8 [R,C], scales fp32 [ceil(R/128), C/128]) from fp32 w [R,C]."""
+    w = _c(w, np.float32)
+    R, C = w.shape
+    q = np.empty((R, C), np.uint8)
+    s = np.empty(((R + 127) // 128, C // 128), np.float32)
+    lib().oracle_quant_128x128_f32(_ptr(w), R, C, _ptr(q), _ptr(s))
+    return q, s
+
+
+def swiglu_backward(h1: np.ndarray, h3: np.ndarray, da: np.ndarray):
+    """(dh1, dh3) in FP64 for a = silu(h1) * h3."""
+    h1, h3, da = _c(h1, np.float64), _c(h3, np.float64), _c(da, np.float64)
+    dh1, dh3 = np.empty_like(h1), np.empty_like(h1)
+    lib().oracle_swiglu_backward(_ptr(h1), _ptr(h3), _ptr(da), h1.size, _ptr(dh1), _ptr(dh3))
+    return dh1, dh3
+
+
+def _f32(w) -> np.ndarray:
+    """fp32 numpy values of a weight given as a torch tensor (bf16 / fp32) or array."""
+    import torch
+    if isinstance(w, torch.Tensor):
+        return w.detach().float().cpu().numpy()
+    return np.asarray(w, np.float32)
+
+
+def _r32(x: np.ndarray) -> np.ndarray:
+    """FP64 -> fp32, one rounding to nearest."""
+    return np.asarray(x, np.float64).astype(np.float32)
+
+
+def _bf(x: np.ndarray) -> np.ndarray:
+    """FP64 values of x rounded once to bf16."""
+    return bf16_value(bf16_round(x))
+
+
+class Backward:
+    """Everything layer_backward computes (FP64 unless stated):
+    h [T,d] (the forward output, before its bf16 rounding), du [T,d],
+    dw1, dw3 [N+1, I, d], dw2 [N+1, d, I], de [N, d], dg, dz [T,K],
+    route (the oracle's routing), rows[e] (token ids of expert e's rows in
+    permuted order) and per-expert intermediates in `inter[e]`."""
+
+
+def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=1, topk_groups=1, fp8=True,
+                   route_all=None) -> Backward:
+    """Gradient of L = sum(G * h') for the layer h' (nlp-lineage page, "The
+    notation") with the expert choice held fixed (readings in moe_oracle.c,
+    [train]):
+
+      combine      dY_r = g_{t,k} G_t (routed row r of (t,k)), dY = G_t (shared),
+                   dg_{t,k} = G_t . y_{row(t,k)}
+      expert e     dA = dY W2,  (dH1, dH3) = SwiGLU'(H1, H3) dA,  dX = dH1 W1 + dH3 W3
+                   dW2 = dY^T A,  dW1 = dH1^T X,  dW3 = dH3^T X   (X = u of the rows)
+      gates        with S = sum_k s_k and c = sum_k g_k dg_k:
+                   dz_{t,k} = (dg_{t,k} - c) / S * s_k (1 - s_k)
+      tokens       du_t = G_t + dX_shared,t + sum_k dX_{row(t,k)} + sum_k dz_{t,k} e_{idx}
+      centroids    de_i = sum over (t,k) routed to i of dz_{t,k} u_t
+
+    fp8=True follows the FP8 path's storage and quantisation points: the
+    forward keeps H = X W13^T (FP8 product) rounded to bf16 and its expert
+    outputs y in bf16; dY is formed in fp32 and quantised per 1x128 tile for
+    dA = dY W2 (W2's forward 128x128 blocks, transposed), dA is stored in bf16;
+    dH is computed from the stored H and dA and stored in bf16, quantised per
+    1x128 tile for dX = dH W13 (bf16 out); the weight gradients quantise both
+    operands per (128 rows of the expert, column) -- dY, A recomputed in fp32
+    from the stored H, dH, and u -- and come out in fp32; du is rounded to
+    bf16 once at the end (the value returned is before that rounding).
+    fp8=False is the same chain with no quantisation and no rounding at all
+    (FP64 throughout), the form the finite-difference pins check.
+
+    expert_weights(e) -> (w1 [I,d], w3 [I,d], w2 [d,I]) as bf16 torch tensors or
+    fp32 arrays; e = N is the shared expert.
+    """
+    import torch
+    u_bits = as_bf16_bits(u_bf16)
+    uv = bf16_value(u_bits)
+    Gv = bf16_value(as_bf16_bits(G_bf16))
+    T, d = uv.shape
+    if isinstance(centroids, torch.Tensor) and centroids.dtype == torch.bfloat16:
+        Ev = bf16_value(as_bf16_bits(centroids))
+    else:
+        Ev = _f32(centroids).astype(np.float64)
+    N = Ev.shape[0]
+    r = route_all if route_all is not None else route(u_bf16, centroids, bias, K, n_groups, topk_groups,
+                                                      want_scores=True)
+    idx, g, s = r.topk_idx, r.gates, r.scores
+    off, perm, dest = permute(idx, N)
+    # gate of each routed row
+    rgate = np.empty(T * K)
+    rgate[dest.ravel()] = g.ravel()
+    out = Backward()
+    out.route, out.offsets, out.perm_token, out.dest_row = r, off, perm, dest
+    out.rows, out.inter = {}, {}
+    I = None
+    Y_rows = np.zeros((T * K, d))
+    Y_sh = None
+    dX_rows = np.zeros((T * K, d))
+    dX_sh = None
+    dW1, dW3, dW2 = [], [], []
+    for e in range(N + 1):
+        w1, w3, w2 = (_f32(w) for w in expert_weights(e))
+        I = w1.shape[0]
+        if e == N:
+            rows = np.arange(T)
+            toks = rows
+            gr = np.ones(T)
+        else:
+            rows = np.arange(off[e], off[e + 1])
+            toks = perm[rows]
+            gr = rgate[rows]
+        out.rows[e] = toks
+        n = toks.size
+        if n == 0:
+            dW1.append(np.zeros((I, d)))
+            dW3.append(np.zeros((I, d)))
+            dW2.append(np.zeros((d, I)))
+            continue
+        X = uv[toks]
+        if fp8:
+            xq, xs = quant_1x128(u_bits[toks])
+            (q1, s1), (q3, s3), (q2, s2) = (quant_128x128_f32(w) for w in (w1, w3, w2))
+            H1, H3 = fp8_gemm(xq, xs, q1, s1), fp8_gemm(xq, xs, q3, s3)
+            aq, as_, _, _ = swiglu_quant(H1, H3)
+            Y = _bf(fp8_gemm(aq, as_, q2, s2))
+            Ht1, Ht3 = _bf(H1), _bf(H3)
+            dY = _r32(gr[:, None] * Gv[toks])
+            qy, sy = quant_1x128_f32(dY)
+            dA = _bf(fp8_gemm(qy, sy, q2.T, s2.T))
+            dH1, dH3 = swiglu_backward(Ht1, Ht3, dA)
+            dHt1, dHt3 = _bf(dH1), _bf(dH3)
+            qh1, sh1 = quant_1x128(bf16_round(dHt1))
+            qh3, sh3 = quant_1x128(bf16_round(dHt3))
+            dX = _bf(fp8_gemm(qh1, sh1, q1.T, s1.T) + fp8_gemm(qh3, sh3, q3.T, s3.T))
+            # weight gradients: operands quantised per (128 rows, column)
+            A32 = _r32(swiglu(Ht1, Ht3))
+            yq_t, ys_t = quant_128x1(dY)
+            aq_t, as_t = quant_128x1(A32)
+            xq_t, xs_t = quant_128x1(X.astype(np.float32))
+            hq1_t, hs1_t = quant_128x1(dHt1.astype(np.float32))
+            hq3_t, hs3_t = quant_128x1(dHt3.astype(np.float32))
+            dW2.append(fp8_gemm_kscaled(yq_t, ys_t, aq_t, as_t))
+            dW1.append(fp8_gemm_kscaled(hq1_t, hs1_t, xq_t, xs_t))
+            dW3.append(fp8_gemm_kscaled(hq3_t, hs3_t, xq_t, xs_t))
+            out.inter[e] = dict(Ht1=Ht1, Ht3=Ht3, Y=Y, dY=dY, dA=dA, dHt1=dHt1, dHt3=dHt3, dX=dX)
+        else:
+            W1, W3, W2 = (w.astype(np.float64) for w in (w1, w3, w2))
+            H1, H3 = X @ W1.T, X @ W3.T
+            A = swiglu(H1, H3)
+            Y = A @ W2.T
+            dY = gr[:, None] * Gv[toks]
+            dA = dY @ W2
+            dH1, dH3 = swiglu_backward(H1, H3, dA)
+            dX = dH1 @ W1 + dH3 @ W3
+            dW2.append(dY.T @ A)
+            dW1.append(dH1.T @ X)
+            dW3.append(dH3.T @ X)
+            out.inter[e] = dict(Ht1=H1, Ht3=H3, Y=Y, dY=dY, dA=dA, dHt1=dH1, dHt3=dH3, dX=dX)
+        if e == N:
+            Y_sh, dX_sh = Y, dX
+        else:
+            Y_rows[rows] = Y
+            dX_rows[rows] = dX
+    rows_tk = dest                                   # [T, K] row of each (t, k)
+    Yk = Y_rows[rows_tk]                             # [T, K, d]
+    out.h = uv + Y_sh + np.einsum("tk,tkd->td", g, Yk)
+    dg = np.einsum("td,tkd->tk", Gv, Yk)
+    s_sel = np.take_along_axis(s, idx.astype(np.int64), axis=1)
+    S = s_sel.sum(axis=1, keepdims=True)
+    c = (g * dg).sum(axis=1, keepdims=True)
+    dz = (dg - c) / S * s_sel * (1.0 - s_sel)
+    du = Gv + dX_sh + dX_rows[rows_tk].sum(axis=1) + np.einsum("tk,tkd->td", dz, Ev[idx])
+    de = np.zeros((N, d))
+    for i in range(N):
+        tt, kk = np.nonzero(idx == i)
+        if tt.size:
+            de[i] = (dz[tt, kk][:, None] * uv[tt]).sum(axis=0)
+    out.du, out.dg, out.dz, out.de = du, dg, dz, de
+    out.dw1, out.dw3, out.dw2 = np.stack(dW1), np.stack(dW3), np.stack(dW2)
+    return out
+
+
+def train_step(u_bf16, masters: dict, bias: np.ndarray, K: int, G_bf16, lr: float, gamma: float, n_groups=1,
+               topk_groups=1):
+    """One training step of the layer (readings in moe_oracle.c, [train], [bias]):
+    the FP8 forward and backward from the fp32 master weights (quantised per
+    128x128 block), plain SGD w <- w - lr * dw on every master in fp32
+    (fl32(w - fl32(lr * dw))), then the load-based bias update.
+
+    masters: {"w1": [N+1, I, d], "w3": [N+1, I, d], "w2": [N+1, d, I],
+    "e": [N, d]} fp32 arrays. Returns (new masters, new bias, Backward)."""
+    m = {k: np.asarray(v, np.float32) for k, v in masters.items()}
+    bw = layer_backward(u_bf16, m["e"], bias, K, lambda e: (m["w1"][e], m["w3"][e], m["w2"][e]), G_bf16,
+                        n_groups=n_groups, topk_groups=topk_groups, fp8=True)
+    lr32 = np.float32(lr)
+    new = {}
+    for k, grad in (("w1", bw.dw1), ("w3", bw.dw3), ("w2", bw.dw2), ("e", bw.de)):
+        step = (lr32 * _r32(grad)).astype(np.float32)
+        new[k] = (m[k] - step).astype(np.float32)
+    T = as_bf16_bits(u_bf16).shape[0]
+    new_bias = bias_update(bias, bw.route.loads, T, K, gamma)
+    return new, new_bias, bw

@@ -1,5 +1,5 @@
 /*
- * FP64 CPU oracle for the DeepSeekMoE layer forward.
+ * FP64 CPU oracle for the DeepSeekMoE layer: forward, backward, training step.
  *
  * TEST INFRASTRUCTURE ONLY. Only the test-suite, the package's smoke check
  * and the benchmark's CPU-baseline leg may load this file's library. It is a
@@ -28,6 +28,11 @@
  *   [seqloss] learn.ifs.name, bias paragraph: beside the bias, only a tiny
  *             sequence-wise balancing loss remains, against extreme
  *             imbalance inside one sequence.
+ *   [train]   nlp-lineage.vercel.app, "The idea", FP8-training item: most
+ *             heavy calculations of training run in 8-bit floating point,
+ *             scaled in small tiles and blocks; learn.ifs.name, DualPipe
+ *             paragraph: each layer has forward and backward chunks; bias
+ *             paragraph: the bias moves after each training step.
  *
  * Readings where the pages are silent (all listed in the design notes):
  *   affinity s = 1/(1+exp(-u.e_i)); gates g = s/sum(s chosen) with factor 1;
@@ -561,5 +566,101 @@ void oracle_seq_balance(const double* scores, const int32_t* topk_idx, int64_t T
             acc += ((double)N * ld[i] / ((double)K * Ts)) * pr[i];
         }
         stat[s] = acc;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass and training step [train]                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Readings (the pages only say that the heavy products of training run in
+ * FP8 with the same fine-grained scaling, and that the bias moves after each
+ * step): the gradient of the layer formula with the expert choice held fixed
+ * and every quantisation or rounding passed straight through; the
+ * backward's products use FP8 operands with the [tiles] rule applied along
+ * their own contraction dimension, promoted every 128 elements [promote].
+ * For a weight gradient the contraction runs over an expert's tokens, so
+ * each operand gets one scale per (128 consecutive rows of the expert,
+ * column): the activation tile turned on its side. */
+
+/* Quantisation for a weight gradient: x fp32 [R, C] (the rows of one expert),
+ * one scale per (block of 128 consecutive rows, column); rows R..Rp-1
+ * (Rp = R rounded up to 128) are zeros. q is stored transposed, [C, Rp]
+ * (K contiguous, as a product operand), scales [Rp/128, C]. */
+void oracle_quant_128x1(const float* x, int64_t R, int64_t C, uint8_t* q, float* scales)
+{
+    tables_init();
+    const int64_t Rp = (R + 127) / 128 * 128, nb = Rp / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < C; ++c) {
+        float col[128];
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int i = 0; i < 128; ++i) {
+                const int64_t r = b * 128 + i;
+                col[i] = r < R ? x[r * C + c] : 0.0f;
+            }
+            scales[b * C + c] = quant_tile(col, 128, 1, q + c * Rp + b * 128, 1);
+        }
+    }
+}
+
+/* Weight-gradient product: both operands scaled per (128-row block, row):
+ *   C[m,n] = sum over blocks b of sa[b,m] * sb[b,n] * sum_{k in b} qa[m,k] * qb[n,k]
+ * qa [M, Kp], qb [Nd, Kp] (K contiguous, Kp % 128 == 0), sa [Kp/128, M],
+ * sb [Kp/128, Nd]; FP64 block sums (exact), FP64 accumulation in block order. */
+void oracle_fp8_gemm_kscaled(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                             int64_t M, int64_t Nd, int64_t Kp, double* C)
+{
+    tables_init();
+    const int64_t nkb = Kp / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < Nd; ++n) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < nkb; ++b) {
+                double part = 0.0;
+                for (int64_t k = b * 128; k < b * 128 + 128; ++k)
+                    part += g_e4m3_all[qa[m * Kp + k]] * g_e4m3_all[qb[n * Kp + k]];
+                acc += (double)sa[b * M + m] * (double)sb[b * Nd + n] * part;
+            }
+            C[m * Nd + n] = acc;
+        }
+}
+
+/* fp32 weights (the training step's master copy): one scale per 128x128
+ * block, the [tiles] rule. Layout as oracle_quant_128x128. */
+void oracle_quant_128x128_f32(const float* w, int64_t rows, int64_t cols, uint8_t* q, float* scales)
+{
+    tables_init();
+    const int64_t nbr = (rows + 127) / 128, nbc = cols / 128;
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t br = 0; br < nbr; ++br) {
+        const int64_t r0 = br * 128, r1 = r0 + 128 < rows ? r0 + 128 : rows;
+        float* buf = (float*)malloc(sizeof(float) * 128 * 128);
+        uint8_t* qb = (uint8_t*)malloc(128 * 128);
+        for (int64_t bc = 0; bc < nbc; ++bc) {
+            int64_t n = 0;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int i = 0; i < 128; ++i) buf[n++] = w[r * cols + bc * 128 + i];
+            scales[br * nbc + bc] = quant_tile(buf, n, 1, qb, 1);
+            n = 0;
+            for (int64_t r = r0; r < r1; ++r)
+                for (int i = 0; i < 128; ++i) q[r * cols + bc * 128 + i] = qb[n++];
+        }
+        free(buf);
+        free(qb);
+    }
+}
+
+/* SwiGLU backward: with a = silu(h1) * h3 and sig = 1/(1+exp(-h1)),
+ *   dh1 = da * h3 * sig * (1 + h1 * (1 - sig)),   dh3 = da * h1 * sig.  FP64. */
+void oracle_swiglu_backward(const double* h1, const double* h3, const double* da, int64_t n, double* dh1,
+                            double* dh3)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const double sig = 1.0 / (1.0 + exp(-h1[i]));
+        dh1[i] = da[i] * h3[i] * sig * (1.0 + h1[i] * (1.0 - sig));
+        dh3[i] = da[i] * h1[i] * sig;
     }
 }
