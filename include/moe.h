@@ -334,6 +334,149 @@ moe_status moe_layer_forward_host_pipelined(const moe_layer_weights* w, const ui
                                             int slot, void* workspace, size_t workspace_bytes, moe_stream_t stream,
                                             void* done_event);
 
+/* ------------------------------------------------------------------------ */
+/* Training: the layer's backward pass and one SGD step.                      */
+/* ------------------------------------------------------------------------ */
+/* Sources: nlp-lineage.vercel.app "DeepSeek-V3 Technical Report (2024)",
+ * "The idea", FP8-training item (the heavy products of training run in
+ * 8-bit floating point, scaled in small tiles and blocks) and "The notation"
+ * (the layer formula); learn.ifs.name "DeepSeek-V3 Technical Report", DualPipe
+ * paragraph (each layer has a forward and a backward chunk: dispatch, MLP,
+ * combine) and bias paragraph (the bias moves after each training step).
+ * Readings (the pages give no formula for the backward): the gradient of
+ *   h'_t = u_t + FFN_shared(u_t) + sum_k g_{t,k} FFN_{idx(t,k)}(u_t)
+ * with the expert choice held fixed and every quantisation or bf16 rounding
+ * passed straight through:
+ *   combine   dY_row(t,k) = g_{t,k} G_t (fp32), dY_shared,t = G_t,
+ *             dg_{t,k} = G_t . y_row(t,k)        (G = dL/dh', bf16)
+ *   expert    dA = dY W2 and dX = dH W13 on the tensor cores, FP8 operands:
+ *             dY and dH per 1x128 tile (the tile rule is scale-invariant, so a
+ *             routed row's dY = g G_t takes G_t's codes and g times its
+ *             scales: no fp32 rounding of g G_t), the weights' forward 128x128 blocks
+ *             transposed; dA, dH and dX stored in bf16; dH from the stored
+ *             bf16 products H of the forward (dh1 = dA h3 s (1 + h1 (1 - s)),
+ *             dh3 = dA h1 s, s = sigmoid(h1));
+ *             dW2 = dY^T A and dW13 = dH^T X contract over the expert's own
+ *             tokens: both operands quantised per (128 tokens, column), A
+ *             recomputed in fp32 from H, X = u of the rows; fp32 out;
+ *   gates     S = sum_k s_k, c = sum_k g_k dg_k, dz_k = (dg_k - c) / S s_k (1 - s_k);
+ *   tokens    du_t = G_t + dX_shared,t + sum_k dX_row(t,k) + sum_k dz_k e_idx(t,k)  (bf16);
+ *   centroids de_i = sum over the (t, k) routed to i of dz_{t,k} u_t  (fp32);
+ *   bias      no gradient: it moves by the load rule after the step.
+ * The training step is plain SGD on fp32 master weights, w <- fl32(w -
+ * fl32(lr dw)), after which the FP8 weights are quantised again. FP8 layers
+ * only; I must be a multiple of 256. */
+
+/* W13 and W2 of a FP8 layer quantised per 128x128 block, transposed (codes and
+ * scale grid), for the backward's products dA = dY W2 and dX = dH W13. */
+typedef struct {
+    uint8_t* w13t;             /* [N+1][d][2I] e4m3 */
+    float* w13t_scales;        /* [N+1][d/128][2I/128] */
+    uint8_t* w2t;              /* [N+1][I][d] */
+    float* w2t_scales;         /* [N+1][I/128][d/128] */
+} moe_layer_weights_t;
+
+/* Gradients written by moe_layer_backward (all device memory). */
+typedef struct {
+    float* dw13;               /* [N+1][2I][d] fp32, rows in W13's interleaved order; required */
+    float* dw2;                /* [N+1][d][I] fp32; required */
+    float* dcentroids;         /* [N][d] fp32; required */
+    float* dz;                 /* [T, K] fp32 gradient of the chosen experts' logits; optional */
+} moe_layer_grads;
+
+/* fp32 master copies of the FP8 layer's expert weights (training step). */
+typedef struct {
+    float* w13;                /* [N+1][2I][d], W13's interleaved row order */
+    float* w2;                 /* [N+1][d][I] */
+} moe_layer_masters;
+
+/* The workspace of a training step: the forward's, plus what the backward
+ * keeps (H, the affinities) and its own intermediates. One workspace serves
+ * moe_layer_forward_train and the moe_layer_backward that follows it. */
+size_t moe_layer_train_workspace_size(const moe_layer_weights* w, int64_t T);
+
+/* moe_layer_forward that also keeps, in the workspace, what the backward
+ * reads: the affinities s [T, N] and GEMM 1's products H [T*K+T, 2I] in bf16. */
+moe_status moe_layer_forward_train(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
+                                   const moe_layer_outputs* outs, int update_bias, void* workspace,
+                                   size_t workspace_bytes, moe_stream_t stream);
+
+/* Backward of the moe_layer_forward_train call that last used `workspace`
+ * (same w, u and T): dout = dL/dh' bf16 [T, d] -> du bf16 [T, d] and grads.
+ * Launch sequence: combine backward, FP8 grouped GEMM dA, SwiGLU backward,
+ * FP8 grouped GEMM dX, gate backward and du, centroid gradient, the
+ * weight-gradient operands, two FP8 weight-gradient GEMMs. */
+moe_status moe_layer_backward(const moe_layer_weights* w, const moe_layer_weights_t* wt, const uint16_t* u,
+                              int64_t T, const uint16_t* dout, uint16_t* du, const moe_layer_grads* grads,
+                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* One training step: moe_layer_forward_train with the bias update, the
+ * backward, then SGD with learning rate lr on m's masters and on the fp32
+ * centroids (w->centroid_dtype must be MOE_DTYPE_F32), re-quantisation of
+ * w13/w2 (+ scales) and of wt from the new masters, and, when
+ * w->centroids_prepared is set, the prepared centroids again. Updates in
+ * place: w->w13, w->w13_scales, w->w2, w->w2_scales, w->centroids,
+ * w->centroids_prepared, w->bias, wt's arrays and m's masters. */
+moe_status moe_layer_train_step(const moe_layer_weights* w, const moe_layer_weights_t* wt,
+                                const moe_layer_masters* m, const uint16_t* u, int64_t T, const uint16_t* dout,
+                                float lr, uint16_t* out, uint16_t* du, const moe_layer_outputs* outs,
+                                const moe_layer_grads* grads, void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
+
+/* Named buffers of the training workspace (for tests and inspection):
+ * byte offset and size of `which` for this w and T, or MOE_ERR_INVALID_ARG. */
+enum {
+    MOE_TRAIN_H = 0,           /* bf16 [R, 2I], R = T*K + T: GEMM 1's products */
+    MOE_TRAIN_SCORES = 1,      /* fp32 [T, N] affinities */
+    MOE_TRAIN_DG = 2,          /* fp32 [T, K] */
+    MOE_TRAIN_DA = 3,          /* bf16 [R, I] */
+    MOE_TRAIN_DH = 4,          /* bf16 [R, 2I] */
+    MOE_TRAIN_DX = 5,          /* bf16 [R, d] */
+    MOE_TRAIN_OFFSETS = 6,     /* int32 [N+2] row offsets of the groups */
+    MOE_TRAIN_PERM_TOKEN = 7,  /* int32 [T*K] */
+    MOE_TRAIN_DEST_ROW = 8,    /* int32 [T, K] */
+    MOE_TRAIN_Y = 9,           /* bf16 [R, d] expert outputs */
+    MOE_TRAIN_KOFS = 10,       /* int32 [N+2] 128-row block offsets of the weight-gradient K layout */
+    MOE_TRAIN_DY_Q = 11,       /* e4m3 [R, d] the operand dY of dA = dY W2 */
+    MOE_TRAIN_DY_S = 12,       /* fp32 [d/128, R] its 1x128 scales */
+    MOE_TRAIN_DH_Q = 13,       /* e4m3 [R, 2I] the operand dH of dX = dH W13 */
+    MOE_TRAIN_DH_S = 14,       /* fp32 [2I/128, R] its 1x128 scales */
+    MOE_TRAIN_ROW_GATE = 15    /* fp32 [R] the gate of each row (1 for the shared expert's) */
+};
+moe_status moe_layer_train_buffer(const moe_layer_weights* w, int64_t T, int which, size_t* offset,
+                                  size_t* bytes);
+
+/* FP8 weight-gradient GEMM, grouped along K: for each group g,
+ *   C[g][m][n] = sum over its 128-K blocks kb of
+ *                sa[kb][m] * sb[kb][n] * sum_{k in kb} A[m][k] * B[n][k]
+ * (each block's partial sum promoted in fp32 with its scales, as in the
+ * forward's products). A e4m3 [M][Kp], B e4m3 [Nd][Kp] (K contiguous),
+ * sa fp32 [Kp/128][M], sb fp32 [Kp/128][Nd], kofs int32 [G+1] device: group
+ * g owns K blocks kofs[g] .. kofs[g+1]-1 (non-decreasing, kofs[0] = 0,
+ * kofs[G] <= Kp/128; a group with no blocks gets zeros). C fp32 [G][M][Nd].
+ * M % 128 == 0, Nd % 256 == 0, Kp % 128 == 0. Bad offsets set
+ * MOE_ERR_DEVICE_DATA in the device status and write nothing. */
+moe_status fp8_grouped_gemm_wgrad(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                                  const int32_t* kofs, int G, int M, int Nd, int64_t Kp, float* C,
+                                  moe_stream_t stream);
+
+/* 128x128-block E4M3 codes and their scales transposed, per group:
+ * q [G][rows][cols], s [G][rows/128][cols/128] -> qt [G][cols][rows],
+ * st [G][cols/128][rows/128]. rows, cols multiples of 128. */
+moe_status fp8_transpose_128x128(const uint8_t* q, const float* s, int G, int rows, int cols, uint8_t* qt,
+                                 float* st, moe_stream_t stream);
+
+/* SGD on an fp32 master [G][rows][cols] and its 128x128 re-quantisation:
+ * w <- fl32(w - fl32(lr * grad)) (two roundings), then per block
+ * scale = amax/448 and q = e4m3(w / scale), stored as is (q [G][rows][cols],
+ * s [G][rows/128][cols/128]) and transposed (qt [G][cols][rows],
+ * st [G][cols/128][rows/128]). rows, cols multiples of 128. */
+moe_status moe_sgd_requant_128x128(float* w, const float* grad, int G, int rows, int cols, float lr, uint8_t* q,
+                                   float* s, uint8_t* qt, float* st, moe_stream_t stream);
+
+/* w <- fl32(w - fl32(lr * grad)) for n fp32 values. */
+moe_status moe_sgd_f32(float* w, const float* grad, int64_t n, float lr, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,6 +28,9 @@ EXPORTS = [
     "moe_route_prepared_centroids_size", "moe_route_prepare_centroids",
     "moe_route_prepared_workspace_size", "moe_route_prepared",
     "moe_route_balance_stats_workspace_size", "moe_route_balance_stats",
+    "moe_layer_train_workspace_size", "moe_layer_forward_train", "moe_layer_backward", "moe_layer_train_step",
+    "moe_layer_train_buffer", "fp8_grouped_gemm_wgrad", "fp8_transpose_128x128", "moe_sgd_requant_128x128",
+    "moe_sgd_f32",
     "moe_permute_workspace_size", "moe_permute", "moe_permute_static",
     "fp8_grouped_gemm", "bf16_grouped_gemm",
     "moe_combine", "moe_bias_update", "moe_selftest_wait_timeout",
@@ -52,6 +55,25 @@ class LayerWeights(ctypes.Structure):
         ("bias", ctypes.c_void_p), ("w13", ctypes.c_void_p), ("w13_scales", ctypes.c_void_p),
         ("w2", ctypes.c_void_p), ("w2_scales", ctypes.c_void_p), ("centroids_prepared", ctypes.c_void_p),
     ]
+
+
+class LayerWeightsT(ctypes.Structure):
+    """moe_layer_weights_t: W13 and W2 quantised per 128x128 block, transposed."""
+    _fields_ = [("w13t", ctypes.c_void_p), ("w13t_scales", ctypes.c_void_p), ("w2t", ctypes.c_void_p),
+                ("w2t_scales", ctypes.c_void_p)]
+
+
+class LayerGrads(ctypes.Structure):
+    _fields_ = [("dw13", ctypes.c_void_p), ("dw2", ctypes.c_void_p), ("dcentroids", ctypes.c_void_p),
+                ("dz", ctypes.c_void_p)]
+
+
+class LayerMasters(ctypes.Structure):
+    _fields_ = [("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p)]
+
+
+TRAIN_BUFFERS = {"H": 0, "scores": 1, "dg": 2, "dA": 3, "dH": 4, "dX": 5, "offsets": 6, "perm_token": 7,
+                 "dest_row": 8, "y": 9, "kofs": 10, "dy_q": 11, "dy_s": 12, "dh_q": 13, "dh_s": 14, "row_gate": 15}
 
 
 class LayerOutputs(ctypes.Structure):
@@ -104,6 +126,20 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_layer_forward_host": (i32, [ctypes.POINTER(LayerWeights), vp, i64, vp,
                                          ctypes.POINTER(LayerOutputs), i32, vp, sz, vp]),
         "moe_layer_host_pipeline_workspace_size": (sz, [ctypes.POINTER(LayerWeights), i64]),
+        "moe_layer_train_workspace_size": (sz, [ctypes.POINTER(LayerWeights), i64]),
+        "moe_layer_forward_train": (i32, [ctypes.POINTER(LayerWeights), vp, i64, vp, ctypes.POINTER(LayerOutputs),
+                                          i32, vp, sz, vp]),
+        "moe_layer_backward": (i32, [ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerWeightsT), vp, i64, vp, vp,
+                                     ctypes.POINTER(LayerGrads), vp, sz, vp]),
+        "moe_layer_train_step": (i32, [ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerWeightsT),
+                                       ctypes.POINTER(LayerMasters), vp, i64, vp, flt, vp, vp,
+                                       ctypes.POINTER(LayerOutputs), ctypes.POINTER(LayerGrads), vp, sz, vp]),
+        "moe_layer_train_buffer": (i32, [ctypes.POINTER(LayerWeights), i64, i32, ctypes.POINTER(sz),
+                                         ctypes.POINTER(sz)]),
+        "fp8_grouped_gemm_wgrad": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i64, vp, vp]),
+        "fp8_transpose_128x128": (i32, [vp, vp, i32, i32, i32, vp, vp, vp]),
+        "moe_sgd_requant_128x128": (i32, [vp, vp, i32, i32, i32, flt, vp, vp, vp, vp, vp]),
+        "moe_sgd_f32": (i32, [vp, vp, i64, flt, vp]),
         "moe_layer_forward_host_pipelined": (i32, [ctypes.POINTER(LayerWeights), vp, i64, vp,
                                                    ctypes.POINTER(LayerOutputs), i32, i32, vp, sz, vp, vp]),
     }
@@ -344,6 +380,50 @@ def moe_bias_update(bias, loads, T, K, gamma):
     _check(load_library().moe_bias_update(_p(bias), _p(loads), bias.numel(), T, K, float(gamma), _stream()),
            "moe_bias_update")
     return bias
+
+
+# --------------------------------------------------------------------------
+# training (include/moe.h, "Training")
+# --------------------------------------------------------------------------
+
+def fp8_grouped_gemm_wgrad(A, sa, B, sb, kofs, out=None):
+    """FP8 weight-gradient GEMM grouped along K: A e4m3 [M, Kp], sa [Kp/128, M],
+    B e4m3 [Nd, Kp], sb [Kp/128, Nd], kofs int32 [G+1] (device, 128-K block
+    offsets of the groups) -> C fp32 [G, M, Nd]."""
+    _require_cuda()
+    M, Kp = A.shape
+    Nd = B.shape[0]
+    G = kofs.numel() - 1
+    out = torch.empty((G, M, Nd), dtype=torch.float32, device=A.device) if out is None else out
+    _check(load_library().fp8_grouped_gemm_wgrad(_p(A), _p(sa), _p(B), _p(sb), _p(kofs), G, M, Nd, Kp, _p(out),
+                                                 _stream()), "fp8_grouped_gemm_wgrad")
+    return out
+
+
+def fp8_transpose_128x128(q, s, qt=None, st=None):
+    """E4M3 codes [G, rows, cols] and 128x128 scales [G, rows/128, cols/128] ->
+    (codes [G, cols, rows], scales [G, cols/128, rows/128])."""
+    _require_cuda()
+    G, rows, cols = q.shape
+    qt = torch.empty((G, cols, rows), dtype=torch.uint8, device=q.device) if qt is None else qt
+    st = torch.empty((G, cols // 128, rows // 128), dtype=torch.float32, device=q.device) if st is None else st
+    _check(load_library().fp8_transpose_128x128(_p(q), _p(s), G, rows, cols, _p(qt), _p(st), _stream()),
+           "fp8_transpose_128x128")
+    return qt, st
+
+
+def moe_sgd_requant_128x128(w, grad, lr, q, s, qt, st):
+    """w [G, rows, cols] fp32 <- fl32(w - fl32(lr grad)); then q, s (128x128
+    E4M3 and scales of the new w) and qt, st (the same, transposed)."""
+    _require_cuda()
+    G, rows, cols = w.shape
+    _check(load_library().moe_sgd_requant_128x128(_p(w), _p(grad), G, rows, cols, float(lr), _p(q), _p(s), _p(qt),
+                                                   _p(st), _stream()), "moe_sgd_requant_128x128")
+
+
+def moe_sgd_f32(w, grad, lr):
+    _require_cuda()
+    _check(load_library().moe_sgd_f32(_p(w), _p(grad), w.numel(), float(lr), _stream()), "moe_sgd_f32")
 
 
 from .layer import MoELayer  # noqa: E402  (after the entry points it wraps)

@@ -232,9 +232,11 @@ moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_
     return MOE_OK;
 }
 
-moe_status fp8_grouped_gemm(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
-                            const int32_t* group_offsets, int G, int64_t M_total, int Nd, int Kd, int epilogue,
-                            void* C, float* c_scales, moe_stream_t stream) {
+// fp8_grouped_gemm; with h_out (MOE_EPI_SWIGLU_FP8 only) the products are also
+// stored in bf16 [M_total, Nd] (the training forward keeps them).
+static moe_status fp8_gemm_impl(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                                const int32_t* group_offsets, int G, int64_t M_total, int Nd, int Kd, int epilogue,
+                                void* C, float* c_scales, uint16_t* h_out, moe_stream_t stream) {
     REQUIRE(G >= 1 && G <= moe::gemm_max_groups(), "fp8_grouped_gemm: G=%d must be in [1, 1024]", G);
     REQUIRE(M_total >= 0 && M_total <= kMaxRows, "fp8_grouped_gemm: M_total out of range");
     REQUIRE(Kd > 0 && Kd % 128 == 0, "fp8_grouped_gemm: Kd=%d must be a multiple of 128", Kd);
@@ -267,8 +269,16 @@ moe_status fp8_grouped_gemm(const uint8_t* A, const float* sa, const uint8_t* B,
     a.sb = sb;
     a.C = C;
     a.c_scales = c_scales;
+    a.h_out = h_out;
+    REQUIRE(!h_out || (epilogue == MOE_EPI_SWIGLU_FP8 && al32(h_out)), "fp8_grouped_gemm: bad product output");
     CUDA_OK(moe::run_grouped_gemm(moe::kModeFP8, ta, tb, a, moe::num_sms(), stream));
     return MOE_OK;
+}
+
+moe_status fp8_grouped_gemm(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
+                            const int32_t* group_offsets, int G, int64_t M_total, int Nd, int Kd, int epilogue,
+                            void* C, float* c_scales, moe_stream_t stream) {
+    return fp8_gemm_impl(A, sa, B, sb, group_offsets, G, M_total, Nd, Kd, epilogue, C, c_scales, nullptr, stream);
 }
 
 moe_status bf16_grouped_gemm(const uint16_t* A, const uint16_t* B, const int32_t* group_offsets, int G,
@@ -393,9 +403,11 @@ size_t moe_layer_host_workspace_size(const moe_layer_weights* w, int64_t T) {
     return w ? layer_ws(w, T, 1).total : 0;
 }
 
+// scores / h_out (training forward, FP8 only): the affinities [T, N] and GEMM 1's
+// products in bf16 [R, 2I] are kept there.
 static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
                                 const moe_layer_outputs* outs, int update_bias, uint8_t* ws, const LayerWs& L,
-                                moe_stream_t stream) {
+                                moe_stream_t stream, float* scores = nullptr, uint16_t* h_out = nullptr) {
     const int K = w->K, N = w->N, d = w->d, I = w->I;
     const int64_t R = T * K + T;
     if (T == 0) {
@@ -419,21 +431,21 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
     STATUS_OK(mark(0));
     if (w->centroids_prepared)
         STATUS_OK(moe_route_prepared(u, T, d, w->centroids_prepared, w->centroid_dtype, w->bias, N, K, w->n_groups,
-                                     w->topk_groups, topk, gates, loads, nullptr, ws + L.route, L.perm - L.route,
+                                     w->topk_groups, topk, gates, loads, scores, ws + L.route, L.perm - L.route,
                                      stream));
     else
         STATUS_OK(moe_route(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups,
-                            topk, gates, loads, nullptr, ws + L.route, L.perm - L.route, stream));
+                            topk, gates, loads, scores, ws + L.route, L.perm - L.route, stream));
     STATUS_OK(mark(1));
     STATUS_OK(moe_permute(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
                           reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,
                           reinterpret_cast<float*>(ws + L.x_scales), ws + L.perm, L.offsets - L.perm, stream));
     STATUS_OK(mark(2));
     if (w->fp8) {
-        STATUS_OK(fp8_grouped_gemm(ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales),
-                                   reinterpret_cast<const uint8_t*>(w->w13), w->w13_scales, offsets, N + 1, R, 2 * I, d,
-                                   MOE_EPI_SWIGLU_FP8, ws + L.act, reinterpret_cast<float*>(ws + L.act_scales),
-                                   stream));
+        STATUS_OK(fp8_gemm_impl(ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales),
+                                reinterpret_cast<const uint8_t*>(w->w13), w->w13_scales, offsets, N + 1, R, 2 * I, d,
+                                MOE_EPI_SWIGLU_FP8, ws + L.act, reinterpret_cast<float*>(ws + L.act_scales), h_out,
+                                stream));
         STATUS_OK(mark(3));
         STATUS_OK(fp8_grouped_gemm(ws + L.act, reinterpret_cast<float*>(ws + L.act_scales),
                                    reinterpret_cast<const uint8_t*>(w->w2), w->w2_scales, offsets, N + 1, R, d, I,

@@ -1,0 +1,592 @@
+// The layer's backward pass and training step: the memory-bound kernels.
+//
+// Sources (the DeepSeek-V3 Technical Report as summarised on the web):
+//   nlp-lineage.vercel.app "DeepSeek-V3 Technical Report (2024)", "The
+//   notation" (the layer formula h'_t = u_t + FFN_shared(u_t) +
+//   sum_k g_{t,k} FFN_{idx}(u_t)) and "The idea", FP8-training item (the heavy
+//   products of training run in FP8 with tile and block scales);
+//   learn.ifs.name "DeepSeek-V3 Technical Report", FP8 paragraph (1x128 tiles,
+//   128x128 blocks) and bias paragraph (the bias moves after each step).
+// Readings: the gradient of the layer formula with the expert choice held
+// fixed; every quantisation and bf16 rounding passed straight through; each
+// backward product takes FP8 operands scaled along its own contraction
+// dimension (a weight gradient contracts over an expert's tokens, so its
+// operands get one scale per 128 tokens and column).
+//
+// Kernels (rows r index the forward's permuted rows: routed rows grouped by
+// expert, then T rows of the shared expert):
+//   combine_bwd     one block per token: dg_{t,k} = G_t . y_{row(t,k)} and the
+//                   dgrad operand dY = g G_t per 1x128 tile (G_t's codes, g times
+//                   its scales)
+//   swiglu_bwd      one warp per (row, 128 outputs): dH from the stored bf16
+//                   H and dA, stored in bf16 and quantised per 1x128 tile
+//   kblock_offsets  each group's first 128-row block in the padded K layout
+//   quant_t         the weight-gradient operands: 128 rows x 64 columns per
+//                   block, transposed, one scale per (128 rows, column)
+//   unpermute_bwd   one block per token: gate backward and du
+//   centroid_grad   de_i = sum over expert i's rows of dz u_t, in row order
+//   fp8_transpose   128x128 E4M3 blocks transposed with their scales
+//   sgd_requant     w <- fl32(w - fl32(lr g)) on fp32 masters, then the
+//                   128x128 quantisation, stored as is and transposed
+// All HBM bound; every sum runs in a fixed order (results reproducible bit for bit).
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x);
+    f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y);
+    f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z);
+    f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w);
+    f[7] = bf16_hi(v.w);
+}
+
+// 8 values of one 1x128 tile (16 lanes hold a tile) -> 8 codes; returns the scale.
+__device__ __forceinline__ float quant8_tile16(const float (&f)[8], uint2& codes) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = tile_scale(amax);
+    codes.x = pack_e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
+              (pack_e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
+    codes.y = pack_e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
+              (pack_e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
+    return sc;
+}
+
+constexpr int kMaxK = 16;
+
+// One block of 256 threads per token t. Thread i takes the 8-column chunks
+// i, i + 256, ... (a 1x128 tile is 16 consecutive threads).
+// The dgrad operand of a routed row is the tile rule applied to g G_t: the
+// rule is scale-invariant (amax and every value scale by g), so its codes are
+// those of G_t's tile and its scale is g times G_t's. G_t's tiles are
+// quantised once and written to the shared expert's row (scale 1 x) and to
+// each of the token's K routed rows (scale g_k x).
+__global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __restrict__ G,
+                                                          const uint16_t* __restrict__ y,
+                                                          const float* __restrict__ gates,
+                                                          const int32_t* __restrict__ dest, int64_t T, int d, int K,
+                                                          int64_t R, uint8_t* __restrict__ qdy,
+                                                          float* __restrict__ sdy, float* __restrict__ row_gate,
+                                                          float* __restrict__ dg) {
+    __shared__ float red[8][kMaxK];
+    const int64_t t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    int64_t rows[kMaxK];
+    float g[kMaxK], acc[kMaxK];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        rows[k] = k < K ? int64_t(__ldg(dest + t * K + k)) : 0;
+        g[k] = k < K ? __ldg(gates + t * K + k) : 0.0f;
+        acc[k] = 0.0f;
+    }
+    const int64_t shared_row = T * K + t;
+    const int chunks = d / 8;
+    for (int c0 = 0; c0 < chunks; c0 += 256) {
+        const int c = c0 + tid;
+        const bool on = c < chunks;   // whole 16-lane tiles are on or off together (d % 128 == 0)
+        float gv[8];
+        {
+            const uint4 v = on ? __ldg(reinterpret_cast<const uint4*>(G + t * d) + c) : make_uint4(0, 0, 0, 0);
+            unpack8(v, gv);
+        }
+        const int64_t col = int64_t(c) * 8;
+        const int64_t kb = col / 128;
+        uint2 codes;
+        const float sc = quant8_tile16(gv, codes);
+        if (on) {
+            *reinterpret_cast<uint2*>(qdy + shared_row * d + col) = codes;
+            if ((lane & 15) == 0) sdy[kb * R + shared_row] = sc;
+        }
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+            if (k >= K) break;
+            float yv[8];
+            const uint4 v = on ? __ldg(reinterpret_cast<const uint4*>(y + rows[k] * d) + c) : make_uint4(0, 0, 0, 0);
+            unpack8(v, yv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[k] = fmaf(gv[i], yv[i], acc[k]);
+            if (on) {
+                *reinterpret_cast<uint2*>(qdy + rows[k] * d + col) = codes;
+                if ((lane & 15) == 0) sdy[kb * R + rows[k]] = __fmul_rn(g[k], sc);
+            }
+        }
+    }
+    // dg: each thread's partial, a fixed xor tree inside the warp, warps in order
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k >= K) break;
+        float v = acc[k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[w][k] = v;
+    }
+    __syncthreads();
+    if (tid < K) {
+        float v = 0.0f;
+        for (int i = 0; i < 8; ++i) v += red[i][tid];
+        dg[t * K + tid] = v;
+        row_gate[__ldg(dest + t * K + tid)] = __ldg(gates + t * K + tid);
+    }
+    if (tid == 0) row_gate[shared_row] = 1.0f;
+}
+
+// One warp per (row r, pair p of 128-column blocks): lanes hold 4 of the 128
+// outputs. H's columns 256p.. are the gate products, 256p+128.. the up ones.
+__global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t* __restrict__ dA,
+                                                         const uint16_t* __restrict__ H, int64_t R, int I,
+                                                         uint16_t* __restrict__ dH, uint8_t* __restrict__ qdh,
+                                                         float* __restrict__ sdh) {
+    const int lane = threadIdx.x & 31;
+    const int pairs = I / 128;
+    const int64_t item = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (item >= R * pairs) return;   // warp-uniform
+    const int64_t r = item / pairs;
+    const int p = int(item - r * pairs);
+    const int I2 = 2 * I;
+    const uint2 va = __ldg(reinterpret_cast<const uint2*>(dA + r * I + 128 * p) + lane);
+    const uint2 v1 = __ldg(reinterpret_cast<const uint2*>(H + r * I2 + 256 * p) + lane);
+    const uint2 v3 = __ldg(reinterpret_cast<const uint2*>(H + r * I2 + 256 * p + 128) + lane);
+    const float a[4] = {bf16_lo(va.x), bf16_hi(va.x), bf16_lo(va.y), bf16_hi(va.y)};
+    const float h1[4] = {bf16_lo(v1.x), bf16_hi(v1.x), bf16_lo(v1.y), bf16_hi(v1.y)};
+    const float h3[4] = {bf16_lo(v3.x), bf16_hi(v3.x), bf16_lo(v3.y), bf16_hi(v3.y)};
+    float d1[4], d3[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float sg = sigmoid_f(h1[i]);
+        d1[i] = a[i] * h3[i] * sg * (1.0f + h1[i] * (1.0f - sg));
+        d3[i] = a[i] * h1[i] * sg;
+    }
+    // stored in bf16; the quantisation below reads the stored values
+    const uint2 b1 = make_uint2(pack_bf16x2(d1[0], d1[1]), pack_bf16x2(d1[2], d1[3]));
+    const uint2 b3 = make_uint2(pack_bf16x2(d3[0], d3[1]), pack_bf16x2(d3[2], d3[3]));
+    reinterpret_cast<uint2*>(dH + r * I2 + 256 * p)[lane] = b1;
+    reinterpret_cast<uint2*>(dH + r * I2 + 256 * p + 128)[lane] = b3;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const uint2 b = half ? b3 : b1;
+        const float f[4] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y)};
+        float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sc = tile_scale(amax);
+        const uint32_t q = pack_e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
+                           (pack_e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
+        reinterpret_cast<uint32_t*>(qdh + r * I2 + 256 * p + 128 * half)[lane] = q;
+        if (lane == 0) sdh[int64_t(2 * p + half) * R + r] = sc;
+    }
+}
+
+// kofs[g] = sum over g' < g of ceil(rows_g' / 128): one warp.
+__global__ void kblock_offsets_kernel(const int32_t* __restrict__ offsets, int G, int32_t* __restrict__ kofs) {
+    const int lane = threadIdx.x;
+    int running = 0;
+    for (int base = 0; base <= G; base += 32) {
+        const int g = base + lane;
+        int blocks = 0;
+        if (g < G) {
+            const int n = offsets[g + 1] - offsets[g];
+            blocks = n > 0 ? (n + 127) / 128 : 0;
+        }
+        int incl = blocks;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (g <= G) kofs[g] = running + incl - blocks;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+}
+
+enum { kSrcScaledG = 0, kSrcTokens = 1, kSrcRows = 2, kSrcSwiglu = 3 };
+
+struct QuantTArgs {
+    const int32_t* offsets;     // [G+1] row offsets of the groups
+    const int32_t* kofs;        // [G+1] their 128-row block offsets (padded)
+    int G;
+    int64_t TK;                 // routed rows; row r >= TK is token r - TK (shared expert)
+    const int32_t* perm_token;  // [TK]
+    const float* row_gate;      // kSrcScaledG: g of each row
+    const uint16_t* src;        // G / u [T, C]; dH [R, C]; H [R, 2C]
+    int C;                      // output rows (columns of the source operand)
+    int64_t Kp;                 // padded rows (row stride of q)
+    uint8_t* q;                 // [C][Kp]
+    float* s;                   // [Kp/128][C]
+};
+
+// One block per (128-row block b of the padded layout, 64 columns): rows of
+// the block gathered into shared memory as fp32, then per column the amax of
+// its 128 rows, the scale and the codes, written transposed.
+template <int kSrc>
+__global__ void __launch_bounds__(256) quant_t_kernel(const QuantTArgs a) {
+    __shared__ float tile[128][65];
+    __shared__ int row_src[128];
+    __shared__ float row_w[128];
+    const int64_t b = blockIdx.x;
+    const int c0 = blockIdx.y * 64;
+    const int tid = threadIdx.x;
+    if (b >= a.kofs[a.G]) return;   // block-uniform
+    if (tid < 32) {
+        // the group of block b (kofs is non-decreasing; find the last g with kofs[g] <= b)
+        int lo = 0, hi = a.G;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (a.kofs[mid] <= b) lo = mid;
+            else hi = mid;
+        }
+        const int64_t r0 = a.offsets[lo] + (b - a.kofs[lo]) * 128;
+        const int64_t r1 = a.offsets[lo + 1];
+        for (int i = tid; i < 128; i += 32) {
+            const int64_t r = r0 + i;
+            int srow = -1;
+            float wgt = 0.0f;
+            if (r < r1) {
+                if (kSrc == kSrcScaledG || kSrc == kSrcTokens) srow = r < a.TK ? a.perm_token[r] : int(r - a.TK);
+                else srow = int(r);
+                if (kSrc == kSrcScaledG) wgt = a.row_gate[r];
+            }
+            row_src[i] = srow;
+            row_w[i] = wgt;
+        }
+    }
+    __syncthreads();
+    // gather: 8 lanes per row (8 bf16 columns each), 32 rows per pass
+    {
+        const int rr = tid >> 3, cc = (tid & 7) * 8;
+        for (int i = rr; i < 128; i += 32) {
+            const int sr = row_src[i];
+            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (sr >= 0) {
+                if (kSrc == kSrcSwiglu) {
+                    // output column c: gate product at 256 (c / 128) + c % 128, up product 128 further
+                    const int c = c0 + cc;
+                    const int64_t base = int64_t(sr) * (2 * a.C) + 256 * (c / 128) + (c % 128);
+                    float h1[8], h3[8];
+                    unpack8(__ldg(reinterpret_cast<const uint4*>(a.src + base)), h1);
+                    unpack8(__ldg(reinterpret_cast<const uint4*>(a.src + base + 128)), h3);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = h1[j] * sigmoid_f(h1[j]) * h3[j];
+                } else {
+                    unpack8(__ldg(reinterpret_cast<const uint4*>(a.src + int64_t(sr) * a.C + c0 + cc)), f);
+                    if (kSrc == kSrcScaledG) {
+                        const float wg = row_w[i];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) f[j] = wg * f[j];
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) tile[i][cc + j] = f[j];
+        }
+    }
+    __syncthreads();
+    // 4 lanes per column, 32 rows each
+    const int col = tid >> 2, qt = tid & 3;
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        v[i] = tile[32 * qt + i][col];
+        amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float sc = tile_scale(amax);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = pack_e4m3x2(__fdiv_rn(v[4 * i], sc), __fdiv_rn(v[4 * i + 1], sc)) |
+               (pack_e4m3x2(__fdiv_rn(v[4 * i + 2], sc), __fdiv_rn(v[4 * i + 3], sc)) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(a.q + int64_t(c0 + col) * a.Kp + b * 128 + 32 * qt);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    if (qt == 0) a.s[b * a.C + c0 + col] = sc;
+}
+
+// One block of 256 threads per token: the gate backward (K scalars, thread 0)
+// and du_t = G_t + dX_shared,t + sum_k dX_row(t,k) + sum_k dz_k e_idx(t,k).
+__global__ void __launch_bounds__(256) unpermute_bwd_kernel(
+    const uint16_t* __restrict__ G, const uint16_t* __restrict__ dX, const int32_t* __restrict__ dest,
+    const int32_t* __restrict__ topk, const float* __restrict__ gates, const float* __restrict__ scores,
+    const float* __restrict__ dg, const void* __restrict__ centroids, int centroid_f32, int64_t T, int d, int N,
+    int K, uint16_t* __restrict__ du, float* __restrict__ dz_row, float* __restrict__ dz_out) {
+    __shared__ float dz[kMaxK];
+    __shared__ int64_t rows[kMaxK];
+    __shared__ int ids[kMaxK];
+    const int64_t t = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        float S = 0.0f, c = 0.0f, s[kMaxK];
+        for (int k = 0; k < K; ++k) {
+            const int e = topk[t * K + k];
+            ids[k] = e;
+            rows[k] = dest[t * K + k];
+            s[k] = scores[t * N + e];
+            S += s[k];
+            c = fmaf(gates[t * K + k], dg[t * K + k], c);
+        }
+        for (int k = 0; k < K; ++k) {
+            const float v = __fdiv_rn(dg[t * K + k] - c, S) * s[k] * (1.0f - s[k]);
+            dz[k] = v;
+            dz_row[rows[k]] = v;
+            if (dz_out) dz_out[t * K + k] = v;
+        }
+    }
+    __syncthreads();
+    const int64_t shared_row = T * K + t;
+    for (int c = tid; c < d / 8; c += 256) {
+        float acc[8], f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(G + t * d) + c), acc);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dX + shared_row * d) + c), f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] += f[j];
+        for (int k = 0; k < K; ++k) {
+            unpack8(__ldg(reinterpret_cast<const uint4*>(dX + rows[k] * d) + c), f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += f[j];
+        }
+        for (int k = 0; k < K; ++k) {
+            const int64_t e = ids[k];
+            if (centroid_f32) {
+                const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(centroids) + e * d) + 2 * c;
+                const float4 x0 = __ldg(p), x1 = __ldg(p + 1);
+                const float ev[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(dz[k], ev[j], acc[j]);
+            } else {
+                unpack8(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(centroids) + e * d) + c), f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(dz[k], f[j], acc[j]);
+            }
+        }
+        reinterpret_cast<uint4*>(du + t * d)[c] =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                       pack_bf16x2(acc[6], acc[7]));
+    }
+}
+
+// Block (expert i, 1024 columns): de[i, cols] = sum over the expert's rows r
+// (ascending) of dz_row[r] * u[token(r), cols].
+__global__ void __launch_bounds__(256) centroid_grad_kernel(const uint16_t* __restrict__ u,
+                                                            const int32_t* __restrict__ offsets,
+                                                            const int32_t* __restrict__ perm_token,
+                                                            const float* __restrict__ dz_row, int d,
+                                                            float* __restrict__ de) {
+    const int i = blockIdx.x;
+    const int col = blockIdx.y * 1024 + threadIdx.x * 4;
+    if (col >= d) return;
+    float acc[4] = {0, 0, 0, 0};
+    const int r0 = offsets[i], r1 = offsets[i + 1];
+    for (int r = r0; r < r1; ++r) {
+        const float w = __ldg(dz_row + r);
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(u + int64_t(__ldg(perm_token + r)) * d + col));
+        acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
+        acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
+        acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
+        acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
+    }
+    *reinterpret_cast<float4*>(de + int64_t(i) * d + col) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+}
+
+// One block per (group, 128x128 block): codes transposed through shared memory.
+__global__ void __launch_bounds__(256) fp8_transpose_kernel(const uint8_t* __restrict__ q, const float* __restrict__ s,
+                                                            int rows, int cols, uint8_t* __restrict__ qt,
+                                                            float* __restrict__ st) {
+    __shared__ uint8_t tile[128][129];
+    const int bc = blockIdx.x, br = blockIdx.y;
+    const int64_t g = blockIdx.z;
+    const int tid = threadIdx.x;
+    const uint8_t* src = q + g * rows * int64_t(cols);
+    uint8_t* dst = qt + g * rows * int64_t(cols);
+    // read: 8 lanes per row of 128 bytes (16 each), 32 rows per pass
+    for (int r = tid >> 3; r < 128; r += 32) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + int64_t(br * 128 + r) * cols + bc * 128) + (tid & 7));
+        const uint8_t* bv = reinterpret_cast<const uint8_t*>(&v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tile[r][(tid & 7) * 16 + j] = bv[j];
+    }
+    __syncthreads();
+    for (int r = tid >> 3; r < 128; r += 32) {
+        uint4 v;
+        uint8_t* bv = reinterpret_cast<uint8_t*>(&v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) bv[j] = tile[(tid & 7) * 16 + j][r];
+        reinterpret_cast<uint4*>(dst + int64_t(bc * 128 + r) * rows + br * 128)[tid & 7] = v;
+    }
+    if (tid == 0) {
+        const int nbr = rows / 128, nbc = cols / 128;
+        st[g * nbr * nbc + int64_t(bc) * nbr + br] = s[g * nbr * nbc + int64_t(br) * nbc + bc];
+    }
+}
+
+// One block per (group, 128x128 block) of an fp32 master [G][rows][cols]:
+// w <- fl32(w - fl32(lr * grad)), then the block's scale amax/448 and codes,
+// stored row-major (q, s [G][rows/128][cols/128]) and transposed (qt [G][cols][rows],
+// st [G][cols/128][rows/128]). Thread t: row t/2, 64 columns.
+__global__ void __launch_bounds__(256) sgd_requant_kernel(float* __restrict__ w, const float* __restrict__ grad,
+                                                          int rows, int cols, float lr, uint8_t* __restrict__ q,
+                                                          float* __restrict__ s, uint8_t* __restrict__ qt,
+                                                          float* __restrict__ st) {
+    __shared__ uint8_t tile[128][129];
+    __shared__ float warp_max[8];
+    const int bc = blockIdx.x, br = blockIdx.y;
+    const int64_t g = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int r = tid >> 1, cbase = (tid & 1) * 64;
+    const int64_t off = g * int64_t(rows) * cols + int64_t(br * 128 + r) * cols + bc * 128 + cbase;
+    float4* wp = reinterpret_cast<float4*>(w + off);
+    const float4* gp = reinterpret_cast<const float4*>(grad + off);
+    float amax = 0.0f;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        float4 x = wp[i];
+        const float4 d = __ldg(gp + i);
+        // two fp32 roundings, never fused: the product, then the difference
+        x.x = __fsub_rn(x.x, __fmul_rn(lr, d.x));
+        x.y = __fsub_rn(x.y, __fmul_rn(lr, d.y));
+        x.z = __fsub_rn(x.z, __fmul_rn(lr, d.z));
+        x.w = __fsub_rn(x.w, __fmul_rn(lr, d.w));
+        wp[i] = x;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((tid & 31) == 0) warp_max[tid >> 5] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
+    const float sc = tile_scale(amax);
+    uint8_t* qrow = q + off;
+#pragma unroll 2
+    for (int i = 0; i < 16; i += 2) {
+        const float4 x0 = wp[i], x1 = wp[i + 1];   // this thread's own stores, read back
+        const uint32_t a0 = pack_e4m3x2(__fdiv_rn(x0.x, sc), __fdiv_rn(x0.y, sc)) |
+                            (pack_e4m3x2(__fdiv_rn(x0.z, sc), __fdiv_rn(x0.w, sc)) << 16);
+        const uint32_t a1 = pack_e4m3x2(__fdiv_rn(x1.x, sc), __fdiv_rn(x1.y, sc)) |
+                            (pack_e4m3x2(__fdiv_rn(x1.z, sc), __fdiv_rn(x1.w, sc)) << 16);
+        reinterpret_cast<uint2*>(qrow)[i / 2] = make_uint2(a0, a1);
+        const int cc = cbase + 4 * i;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            tile[r][cc + j] = uint8_t(a0 >> (8 * j));
+            tile[r][cc + 4 + j] = uint8_t(a1 >> (8 * j));
+        }
+    }
+    __syncthreads();
+    uint8_t* dst = qt + g * int64_t(rows) * cols;
+    for (int c = tid >> 3; c < 128; c += 32) {
+        uint4 v;
+        uint8_t* bv = reinterpret_cast<uint8_t*>(&v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) bv[j] = tile[(tid & 7) * 16 + j][c];
+        reinterpret_cast<uint4*>(dst + int64_t(bc * 128 + c) * rows + br * 128)[tid & 7] = v;
+    }
+    if (tid == 0) {
+        const int nbr = rows / 128, nbc = cols / 128;
+        s[g * nbr * nbc + int64_t(br) * nbc + bc] = sc;
+        st[g * nbr * nbc + int64_t(bc) * nbr + br] = sc;
+    }
+}
+
+__global__ void __launch_bounds__(256) sgd_f32_kernel(float* __restrict__ w, const float* __restrict__ grad, int64_t n,
+                                                      float lr) {
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
+        w[i] = __fsub_rn(w[i], __fmul_rn(lr, __ldg(grad + i)));
+}
+
+int grid_for(int64_t items, int per_block) {
+    int64_t b = (items + per_block - 1) / per_block;
+    const int64_t cap = int64_t(num_sms()) * 16;
+    return int(b < 1 ? 1 : (b > cap ? cap : b));
+}
+
+}  // namespace
+
+cudaError_t launch_combine_bwd(const uint16_t* G, const uint16_t* y, const float* gates, const int32_t* dest,
+                               int64_t T, int d, int K, int64_t R, uint8_t* qdy, float* sdy, float* row_gate,
+                               float* dg, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    combine_bwd_kernel<<<unsigned(T), 256, 0, stream>>>(G, y, gates, dest, T, d, K, R, qdy, sdy, row_gate, dg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd(const uint16_t* dA, const uint16_t* H, int64_t R, int I, uint16_t* dH, uint8_t* qdh,
+                              float* sdh, cudaStream_t stream) {
+    const int64_t warps = R * (I / 128);
+    if (warps == 0) return cudaSuccess;
+    swiglu_bwd_kernel<<<unsigned((warps + 7) / 8), 256, 0, stream>>>(dA, H, R, I, dH, qdh, sdh);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kblock_offsets(const int32_t* offsets, int G, int32_t* kofs, cudaStream_t stream) {
+    kblock_offsets_kernel<<<1, 32, 0, stream>>>(offsets, G, kofs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_t(int src_kind, const int32_t* offsets, const int32_t* kofs, int G, int64_t TK,
+                           const int32_t* perm_token, const float* row_gate, const uint16_t* src, int C,
+                           int64_t Kp, uint8_t* q, float* s, cudaStream_t stream) {
+    QuantTArgs a{offsets, kofs, G, TK, perm_token, row_gate, src, C, Kp, q, s};
+    const dim3 grid(unsigned(Kp / 128), unsigned(C / 64));
+    if (grid.x == 0) return cudaSuccess;
+    switch (src_kind) {
+        case kSrcScaledG: quant_t_kernel<kSrcScaledG><<<grid, 256, 0, stream>>>(a); break;
+        case kSrcTokens: quant_t_kernel<kSrcTokens><<<grid, 256, 0, stream>>>(a); break;
+        case kSrcRows: quant_t_kernel<kSrcRows><<<grid, 256, 0, stream>>>(a); break;
+        case kSrcSwiglu: quant_t_kernel<kSrcSwiglu><<<grid, 256, 0, stream>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute_bwd(const uint16_t* G, const uint16_t* dX, const int32_t* dest, const int32_t* topk,
+                                 const float* gates, const float* scores, const float* dg, const void* centroids,
+                                 int centroid_f32, int64_t T, int d, int N, int K, uint16_t* du, float* dz_row,
+                                 float* dz_out, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    unpermute_bwd_kernel<<<unsigned(T), 256, 0, stream>>>(G, dX, dest, topk, gates, scores, dg, centroids,
+                                                          centroid_f32, T, d, N, K, du, dz_row, dz_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_centroid_grad(const uint16_t* u, const int32_t* offsets, const int32_t* perm_token,
+                                 const float* dz_row, int N, int d, float* de, cudaStream_t stream) {
+    const dim3 grid(unsigned(N), unsigned((d + 1023) / 1024));
+    centroid_grad_kernel<<<grid, 256, 0, stream>>>(u, offsets, perm_token, dz_row, d, de);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_transpose(const uint8_t* q, const float* s, int G, int rows, int cols, uint8_t* qt, float* st,
+                                 cudaStream_t stream) {
+    const dim3 grid(unsigned(cols / 128), unsigned(rows / 128), unsigned(G));
+    fp8_transpose_kernel<<<grid, 256, 0, stream>>>(q, s, rows, cols, qt, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sgd_requant(float* w, const float* grad, int G, int rows, int cols, float lr, uint8_t* q, float* s,
+                               uint8_t* qt, float* st, cudaStream_t stream) {
+    const dim3 grid(unsigned(cols / 128), unsigned(rows / 128), unsigned(G));
+    sgd_requant_kernel<<<grid, 256, 0, stream>>>(w, grad, rows, cols, lr, q, s, qt, st);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sgd_f32(float* w, const float* grad, int64_t n, float lr, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    sgd_f32_kernel<<<grid_for(n, 256), 256, 0, stream>>>(w, grad, n, lr);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

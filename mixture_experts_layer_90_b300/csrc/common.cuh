@@ -110,6 +110,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+// 16 bytes; both addresses 16-byte aligned
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 // Arrives on `bar` (without raising its expected count) once every cp.async
 // this thread issued so far has landed in shared memory.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -1,6 +1,6 @@
 // Grouped GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// One persistent, warp-specialised kernel serves three uses:
+// One persistent, warp-specialised kernel serves four uses:
 //   * FP8 expert GEMMs with fine-grained scales (DeepSeek-V3 Technical Report,
 //     learn.ifs.name summary, paragraphs on FP8 tiles and on promotion): each
 //     128-wide K block is multiplied by the tensor cores into its own TMEM
@@ -10,6 +10,11 @@
 //   * bf16 expert GEMMs (TMEM partial sums of 8 K steps added into FP32
 //     registers).
 //   * the gate logits of routing (bf16, split-K partial sums in fp32).
+//   * FP8 weight gradients of the layer's backward pass (the groups split K,
+//     not M: each expert's tokens are its own K range, padded to 128; both
+//     operands carry one scale per (128-token block, row), so each 128-K
+//     partial sum is multiplied by sa[row,kb] * sb[col,kb] before it is added
+//     into fp32 registers).
 //
 // Block roles (608 threads):
 //   warps 0-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows); in
@@ -24,6 +29,8 @@
 //               never waits on a global load inside its promotion loop.
 // Tile: 128 rows x 256 columns, K step 128 bytes (128 e4m3 or 64 bf16),
 // 4-stage shared-memory ring (48 KB per stage), 2 x 256 TMEM columns.
+// The SwiGLU FP8 epilogue can also store the tile's fp32 products rounded to
+// bf16 (the training forward keeps them for the backward pass).
 #include "common.cuh"
 #include "gemm.cuh"
 
@@ -39,11 +46,15 @@ constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1, kScaleWarp = 
 constexpr int kMaxGroups = 1024;
 constexpr int kSSlots = 8;   // K blocks of scales staged ahead of the epilogue
 
-struct ScaleSlot {
-    float sa[kBM];   // activation scale of each row of the tile, this K block
-    float sb[4];     // weight scales of the tile's two 128-column blocks (+ pad)
+// kSbN: FP8 forward, the weight scales of the tile's two 128-column blocks
+// (+ pad); weight gradient, one scale per column of the tile.
+template <int kSbN>
+struct alignas(16) ScaleSlot {   // 16-byte cp.async destinations, float2 reads
+    float sa[kBM];   // scale of each row of the tile, this K block
+    float sb[kSbN];
 };
 
+template <int kMode>
 struct Smem {
     uint64_t full[kStages], empty[kStages];
     uint64_t sfull[kSSlots], sempty[kSSlots];
@@ -52,18 +63,25 @@ struct Smem {
     int abort;
     int total_items;
     float amax[2][4][128];
-    ScaleSlot scales[kSSlots];
+    ScaleSlot<kMode == kModeFP8W ? kBN : 4> scales[kSSlots];
     int prefix[kMaxGroups + 1];
-    int offs[kMaxGroups + 1];
+    int offs[kMaxGroups + 1];   // row offsets of the groups (weight gradient: K-block offsets)
 };
 constexpr size_t kRingBytes = size_t(kStages) * (kABytes + kBBytes);
-constexpr size_t kSmemBytes = kRingBytes + sizeof(Smem) + 1024;
+template <int kMode>
+constexpr size_t smem_bytes() {
+    return kRingBytes + sizeof(Smem<kMode>) + 1024;
+}
+static_assert(smem_bytes<kModeFP8W>() <= 227 * 1024, "shared memory");
+static_assert(offsetof(Smem<kModeFP8W>, scales) % 16 == 0 && sizeof(ScaleSlot<kBN>) % 16 == 0, "scale slots");
 
 struct Item {
     int g, mt, nt, sp;
 };
 
-__device__ __forceinline__ Item decode(int item, const Smem& s, int G, int n_tiles_n, int splits) {
+// m_tiles_fixed > 0: every group has that many row tiles (weight gradient)
+template <class S>
+__device__ __forceinline__ Item decode(int item, const S& s, int G, int n_tiles_n, int splits, int m_tiles_fixed = 0) {
     int lo = 0, hi = G;  // prefix[lo] <= item < prefix[hi]
     while (hi - lo > 1) {
         int mid = (lo + hi) >> 1;
@@ -75,7 +93,7 @@ __device__ __forceinline__ Item decode(int item, const Smem& s, int G, int n_til
     int local = item - s.prefix[lo];
     it.sp = local % splits;
     local /= splits;
-    int m_tiles = (s.offs[lo + 1] - s.offs[lo] + kBM - 1) / kBM;
+    int m_tiles = m_tiles_fixed > 0 ? m_tiles_fixed : (s.offs[lo + 1] - s.offs[lo] + kBM - 1) / kBM;
     it.mt = local % m_tiles;
     it.nt = local / m_tiles;
     return it;
@@ -98,7 +116,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem& s = *reinterpret_cast<Smem*>(ring + kRingBytes);
+    Smem<kMode>& s = *reinterpret_cast<Smem<kMode>*>(ring + kRingBytes);
+    constexpr bool kW = kMode == kModeFP8W;         // weight gradient: groups split K
+    constexpr bool kScaled = kMode != kModeBF16;     // FP8 operands with scales
     const uint32_t ringA = smem_u32(ring);
     const uint32_t ringB = ringA + kStages * kABytes;
 
@@ -107,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tiles_n = args.Nd / kBN;
     const int splits = args.splits;
     const int steps_per_split = (args.k_steps + splits - 1) / splits;
+    const int m_fixed = kW ? int(args.M_total / kBM) : 0;
     volatile int* abort = &s.abort;
 
     // ---------------- prologue ----------------
@@ -152,8 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (g < G) {
                 int nxt = args.group_offsets ? args.group_offsets[g + 1] : (int)args.M_total;
                 int rows = nxt - off;
-                if (rows < 0 || off < 0 || nxt > args.M_total) bad = true;
-                items = rows > 0 ? ((rows + kBM - 1) / kBM) * n_tiles_n * splits : 0;
+                if (kW) {
+                    // K-block offsets; every group owns all M/128 x Nd/256 output tiles
+                    // (a group without tokens writes zeros)
+                    if (rows < 0 || off < 0 || nxt > args.k_steps) bad = true;
+                    items = m_fixed * n_tiles_n;
+                } else {
+                    if (rows < 0 || off < 0 || nxt > args.M_total) bad = true;
+                    items = rows > 0 ? ((rows + kBM - 1) / kBM) * n_tiles_n * splits : 0;
+                }
             }
             int incl = items;
 #pragma unroll
@@ -185,11 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int armed[kStages] = {0, 0, 0, 0};
             bool stop = false;
             for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
-                const Item it = decode(item, s, G, n_tiles_n, splits);
-                const int a_row = s.offs[it.g] + it.mt * kBM;
-                const int b_row = it.g * args.Nd + it.nt * kBN;
-                const int k0 = it.sp * steps_per_split;
-                const int k1 = min(args.k_steps, k0 + steps_per_split);
+                const Item it = decode(item, s, G, n_tiles_n, splits, m_fixed);
+                const int a_row = kW ? it.mt * kBM : s.offs[it.g] + it.mt * kBM;
+                const int b_row = kW ? it.nt * kBN : it.g * args.Nd + it.nt * kBN;
+                // weight gradient: the group's own K blocks, at its K-block offset
+                const int kbase = kW ? s.offs[it.g] : 0;
+                const int k0 = kW ? 0 : it.sp * steps_per_split;
+                const int k1 = kW ? s.offs[it.g + 1] - s.offs[it.g] : min(args.k_steps, k0 + steps_per_split);
                 int ka = k0 / args.a_k_repeat;   // A's K step
                 int rep = k0 - ka * args.a_k_repeat;
                 for (int ks = k0; ks < k1; ++ks) {
@@ -199,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t fb = smem_u32(&s.full[stage]);
                     mbar_arrive_expect_tx(fb, kABytes + kBBytes);
-                    tma_load_2d(ringA + stage * kABytes, &tmA, fb, ka * args.elems_per_step, a_row);
-                    tma_load_2d(ringB + stage * kBBytes, &tmB, fb, ks * args.elems_per_step, b_row);
+                    tma_load_2d(ringA + stage * kABytes, &tmA, fb, (kbase + ka) * args.elems_per_step, a_row);
+                    tma_load_2d(ringB + stage * kBBytes, &tmB, fb, (kbase + ks) * args.elems_per_step, b_row);
                     armed[stage] += 1;
                     if (++rep == args.a_k_repeat) {
                         rep = 0;
@@ -220,7 +250,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kScaleWarp) {
         // ---------------- FP8 scales: each K block's 128 row scales and 2 weight scales ----------------
         // copied into the shared ring by all 32 lanes (cp.async), ahead of the epilogue
-        if (kMode == kModeFP8) {
+        if constexpr (kW) {
+            // weight gradient: 128 row scales and 256 column scales per K block, 16-byte copies
+            int sslot = 0;
+            uint32_t sphase = 0;
+            bool stop = false;
+            for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+                const Item it = decode(item, s, G, n_tiles_n, splits, m_fixed);
+                const float* sa_src = args.sa + it.mt * kBM + 4 * lane;
+                const float* sb_src = args.sb + it.nt * kBN + 8 * lane;
+                const int kb0 = s.offs[it.g], kb1 = s.offs[it.g + 1];
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    int ok = 1;
+                    if (lane == 0) ok = mbar_wait(smem_u32(&s.sempty[sslot]), sphase ^ 1u, abort);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        stop = true;
+                        break;
+                    }
+                    cp_async_16(smem_u32(&s.scales[sslot].sa[4 * lane]), sa_src + int64_t(kb) * args.lda_s);
+                    const float* sbk = sb_src + int64_t(kb) * args.Nd;
+                    cp_async_16(smem_u32(&s.scales[sslot].sb[8 * lane]), sbk);
+                    cp_async_16(smem_u32(&s.scales[sslot].sb[8 * lane + 4]), sbk + 4);
+                    cp_async_arrive_noinc(smem_u32(&s.sfull[sslot]));
+                    if (++sslot == kSSlots) {
+                        sslot = 0;
+                        sphase ^= 1u;
+                    }
+                }
+            }
+            cp_async_wait_all();   // no copy into shared memory may outlive the block
+        } else if constexpr (kMode == kModeFP8) {
             int sslot = 0;
             uint32_t sphase = 0;
             const int nkb = args.Kd / 128;
@@ -268,15 +327,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- tcgen05.mma issuer: lane 0 alone ----------------
         // Only lane 0 waits and issues, so a wait that gives up cannot split the warp.
         if (lane == 0) {
-            constexpr uint32_t idesc = kMode == kModeFP8 ? make_idesc(0, 0, kBM, kBN) : make_idesc(1, 1, kBM, kBN);
-            const int P = kMode == kModeFP8 ? 1 : args.promote_steps;
+            constexpr uint32_t idesc = kScaled ? make_idesc(0, 0, kBM, kBN) : make_idesc(1, 1, kBM, kBN);
+            const int P = kScaled ? 1 : args.promote_steps;
             int stage = 0;
             uint32_t phase = 0;
             uint32_t acc_iter = 0;
             for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
-                Item it = decode(item, s, G, n_tiles_n, splits);
-                const int k0 = it.sp * steps_per_split;
-                const int k1 = min(args.k_steps, k0 + steps_per_split);
+                Item it = decode(item, s, G, n_tiles_n, splits, m_fixed);
+                const int k0 = kW ? 0 : it.sp * steps_per_split;
+                const int k1 = kW ? s.offs[it.g + 1] - s.offs[it.g] : min(args.k_steps, k0 + steps_per_split);
                 uint32_t buf = acc_iter & 1u;
                 bool ok = true;
                 for (int ks = k0; ks < k1; ++ks) {
@@ -301,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t acc = (k > 0 || !first) ? 1u : 0u;
-                        if (kMode == kModeFP8) mma_e4m3(d, ad + 2 * k, bd + 2 * k, idesc, acc);
+                        if (kScaled) mma_e4m3(d, ad + 2 * k, bd + 2 * k, idesc, acc);
                         else mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, acc);
                     }
                     tc_commit(smem_u32(&s.empty[stage]));
@@ -338,13 +397,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int item = blockIdx.x; item < total && !*abort; item += gridDim.x) {
             int k0, k1;
             {
-                const Item it = decode(item, s, G, n_tiles_n, splits);
-                k0 = it.sp * steps_per_split;
-                k1 = min(args.k_steps, k0 + steps_per_split);
+                const Item it = decode(item, s, G, n_tiles_n, splits, m_fixed);
+                k0 = kW ? 0 : it.sp * steps_per_split;
+                k1 = kW ? s.offs[it.g + 1] - s.offs[it.g] : min(args.k_steps, k0 + steps_per_split);
             }
             float acc[64];
             bool ok = true;
-            if (kMode == kModeFP8) {
+            if constexpr (kW) {
+                // weight gradient: each 128-K block's partial sums times
+                // sa[row, kb] * sb[col, kb] (one scale per column), added into fp32 registers
+                float2 acc2[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+                for (int ks = k0; ks < k1; ++ks) {
+                    bool got = mbar_wait(smem_u32(&s.sfull[sslot]), sphase, abort);
+                    const uint32_t buf = acc_iter & 1u;
+                    got = got && mbar_wait(smem_u32(&s.tfull[buf]), (acc_iter >> 1) & 1u, abort);
+                    if (!__all_sync(0xffffffffu, got)) {   // warp-collective TMEM loads follow
+                        ok = false;
+                        break;
+                    }
+                    const float sa_v = s.scales[sslot].sa[row_in_tile];
+                    const float2 sa2 = make_float2(sa_v, sa_v);
+                    tc_fence_after();
+                    const uint32_t col = lane_addr + buf * kBN + slice;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[16];
+                        tmem_ld_16(col + c * 16, r);
+                        tmem_wait_ld(r);
+                        if (c == 3) {
+                            tc_fence_before();
+                            mbar_arrive(smem_u32(&s.tempty[buf]));
+                        }
+                        const float2* sbp = reinterpret_cast<const float2*>(&s.scales[sslot].sb[slice + 16 * c]);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float2 f2 = __fmul2_rn(sbp[i], sa2);
+                            acc2[c * 8 + i] = __ffma2_rn(
+                                make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), f2,
+                                acc2[c * 8 + i]);
+                        }
+                    }
+                    // the slot is released after the last column scale was read
+                    mbar_arrive(smem_u32(&s.sempty[sslot]));
+                    if (++sslot == kSSlots) {
+                        sslot = 0;
+                        sphase ^= 1u;
+                    }
+                    acc_iter += 1;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    acc[2 * i] = acc2[i].x;
+                    acc[2 * i + 1] = acc2[i].y;
+                }
+            } else if constexpr (kMode == kModeFP8) {
                 // promotion (accumulation paragraph): each 128-K block's partial sums,
                 // times sa[row, kb] * sb[nblk, kb], added into fp32 registers
                 float2 acc2[32];
@@ -442,12 +550,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---- epilogue of the tile (tile coordinates decoded again: fewer live registers) ----
-            const Item it = decode(item, s, G, n_tiles_n, splits);
+            const Item it = decode(item, s, G, n_tiles_n, splits, m_fixed);
             const int row_local = it.mt * kBM + row_in_tile;
-            const bool valid = row_local < s.offs[it.g + 1] - s.offs[it.g];
-            const int64_t grow = int64_t(s.offs[it.g]) + row_local;
+            // weight gradient: group g's output is rows g*M .. g*M+M-1 of C, all of them written
+            const bool valid = kW || row_local < s.offs[it.g + 1] - s.offs[it.g];
+            const int64_t grow = kW ? int64_t(it.g) * args.M_total + row_local : int64_t(s.offs[it.g]) + row_local;
             constexpr int ep = kEpi;
             if constexpr (ep == MOE_EPI_SWIGLU_FP8 || ep == MOE_EPI_SWIGLU_BF16) {
+                if (ep == MOE_EPI_SWIGLU_FP8 && args.h_out && valid) {
+                    // the products themselves, rounded to bf16, at their columns of the
+                    // [M_total, Nd] product (gate columns, then the up columns 128 further)
+                    uint16_t* hrow = args.h_out + grow * args.Nd + int64_t(it.nt) * kBN + wg * 32;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int v = 0; v < 2; ++v) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                w[i] = pack_bf16x2(acc[32 * half + 16 * v + 2 * i], acc[32 * half + 16 * v + 2 * i + 1]);
+                            st_global_32B(hrow + 128 * half + 16 * v, w);
+                        }
+                }
                 float a[32];
                 float amax = 0.0f;
 #pragma unroll
@@ -584,6 +708,7 @@ template <int kMode, int kEpi>
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
                           cudaStream_t stream) {
     static PerDeviceOnce once;
+    constexpr size_t kSmemBytes = smem_bytes<kMode>();
     cudaError_t e = allow_smem(once, grouped_gemm_kernel<kMode, kEpi>, int(kSmemBytes));
     if (e != cudaSuccess) return e;
     grouped_gemm_kernel<kMode, kEpi><<<grid, kThreads, kSmemBytes, stream>>>(a, b, args);
@@ -592,6 +717,10 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Gemm
 
 cudaError_t run_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
                              cudaStream_t stream) {
+    if (mode == kModeFP8W) {
+        if (args.epilogue == MOE_EPI_F32) return launch<kModeFP8W, MOE_EPI_F32>(a, b, args, grid, stream);
+        return cudaErrorInvalidValue;
+    }
     if (mode == kModeFP8) {
         if (args.epilogue == MOE_EPI_SWIGLU_FP8) return launch<kModeFP8, MOE_EPI_SWIGLU_FP8>(a, b, args, grid, stream);
         if (args.epilogue == MOE_EPI_BF16) return launch<kModeFP8, MOE_EPI_BF16>(a, b, args, grid, stream);

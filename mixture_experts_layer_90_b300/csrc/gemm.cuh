@@ -7,7 +7,9 @@
 
 namespace moe {
 
-enum { kModeFP8 = 0, kModeBF16 = 1 };
+// kModeFP8W: FP8 weight gradient, groups split K (group_offsets in 128-K blocks),
+// scales per (K block, row of A) and per (K block, row of B), fp32 output [G][M][Nd].
+enum { kModeFP8 = 0, kModeBF16 = 1, kModeFP8W = 2 };
 
 // bf16 GEMMs add their TMEM partial sums into fp32 registers every this many
 // 64-wide K steps (512 products): a long fp32 accumulation in the tensor
@@ -29,9 +31,10 @@ struct GemmArgs {
     int epilogue;        // MOE_EPI_*
     const float* sa;     // FP8: [Kd/128][lda_s] activation scales
     int64_t lda_s;
-    const float* sb;     // FP8: [G][Nd/128][Kd/128] weight scales
+    const float* sb;     // FP8: [G][Nd/128][Kd/128] weight scales; FP8W: [Kd/128][Nd]
     void* C;
     float* c_scales;     // MOE_EPI_SWIGLU_FP8: [Nd/256][M_total]
+    uint16_t* h_out;     // MOE_EPI_SWIGLU_FP8, optional: the fp32 products rounded to bf16 [M_total][Nd]
 };
 
 bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inner, uint64_t rows,

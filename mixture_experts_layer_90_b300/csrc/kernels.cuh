@@ -45,6 +45,29 @@ cudaError_t launch_combine(const uint16_t* u, const uint16_t* y_shared, const ui
                            const int32_t* dest_row, int64_t T, int d, int K, int64_t R, uint16_t* out,
                            cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+// Backward pass and training step (backward.cu).
+enum { kQuantTScaledG = 0, kQuantTTokens = 1, kQuantTRows = 2, kQuantTSwiglu = 3 };
+cudaError_t launch_combine_bwd(const uint16_t* G, const uint16_t* y, const float* gates, const int32_t* dest,
+                               int64_t T, int d, int K, int64_t R, uint8_t* qdy, float* sdy, float* row_gate,
+                               float* dg, cudaStream_t stream);
+cudaError_t launch_swiglu_bwd(const uint16_t* dA, const uint16_t* H, int64_t R, int I, uint16_t* dH, uint8_t* qdh,
+                              float* sdh, cudaStream_t stream);
+cudaError_t launch_kblock_offsets(const int32_t* offsets, int G, int32_t* kofs, cudaStream_t stream);
+cudaError_t launch_quant_t(int src_kind, const int32_t* offsets, const int32_t* kofs, int G, int64_t TK,
+                           const int32_t* perm_token, const float* row_gate, const uint16_t* src, int C,
+                           int64_t Kp, uint8_t* q, float* s, cudaStream_t stream);
+cudaError_t launch_unpermute_bwd(const uint16_t* G, const uint16_t* dX, const int32_t* dest, const int32_t* topk,
+                                 const float* gates, const float* scores, const float* dg, const void* centroids,
+                                 int centroid_f32, int64_t T, int d, int N, int K, uint16_t* du, float* dz_row,
+                                 float* dz_out, cudaStream_t stream);
+cudaError_t launch_centroid_grad(const uint16_t* u, const int32_t* offsets, const int32_t* perm_token,
+                                 const float* dz_row, int N, int d, float* de, cudaStream_t stream);
+cudaError_t launch_fp8_transpose(const uint8_t* q, const float* s, int G, int rows, int cols, uint8_t* qt, float* st,
+                                 cudaStream_t stream);
+cudaError_t launch_sgd_requant(float* w, const float* grad, int G, int rows, int cols, float lr, uint8_t* q, float* s,
+                               uint8_t* qt, float* st, cudaStream_t stream);
+cudaError_t launch_sgd_f32(float* w, const float* grad, int64_t n, float lr, cudaStream_t stream);
 cudaError_t launch_bias_update(float* bias, const int32_t* loads, int N, int64_t T, int K, float gamma,
                                cudaStream_t stream);
 

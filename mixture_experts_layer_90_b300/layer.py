@@ -10,6 +10,11 @@ Layout (all device memory, allocated once here, never by the C library):
                     (gate rows 128j.., then up rows 128j..), expert N = shared
   w2  [N+1, d, I]   down projections
   *_scales          fp32 [N+1, rows/128, cols/128]
+
+Training (FP8 layers; enable_training or build(..., train=True)) adds fp32
+masters of w13 and w2, their FP8 codes transposed per 128x128 block (w13t
+[N+1, d, 2I], w2t [N+1, I, d], for the backward's products) and the
+gradients dw13, dw2 (fp32, the masters' layouts) and dcentroids [N, d].
 """
 from __future__ import annotations
 
@@ -17,8 +22,9 @@ import ctypes
 
 import torch
 
-from . import (MOE_DTYPE_BF16, MOE_DTYPE_F32, LayerOutputs, LayerWeights, _check, _p, _require_cuda, _stream,
-               fp8_quant_128x128, load_library, moe_route_prepare_centroids)
+from . import (MOE_DTYPE_BF16, MOE_DTYPE_F32, TRAIN_BUFFERS, LayerGrads, LayerMasters, LayerOutputs, LayerWeights,
+               LayerWeightsT, _check, _p, _require_cuda, _stream, fp8_quant_128x128, fp8_transpose_128x128,
+               load_library, moe_route_prepare_centroids)
 
 
 def interleave_gate_up(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
@@ -50,11 +56,15 @@ class MoELayer:
         self.loads = torch.zeros((N,), dtype=torch.int32, device=centroids.device)
 
     @classmethod
-    def build(cls, d, N, K, I, centroids, bias, expert_weights, fp8=True, **kw):
+    def build(cls, d, N, K, I, centroids, bias, expert_weights, fp8=True, train=False, **kw):
         """expert_weights(e) -> (w1 [I,d], w3 [I,d], w2 [d,I]) bf16 device tensors for
-        e in 0..N (N = shared expert); quantised here per 128x128 block when fp8."""
+        e in 0..N (N = shared expert); quantised here per 128x128 block when fp8.
+        train: also keep fp32 masters of the weights and set up training."""
         dev = centroids.device
         G = N + 1
+        if train:
+            w13m = torch.empty((G, 2 * I, d), dtype=torch.float32, device=dev)
+            w2m = torch.empty((G, d, I), dtype=torch.float32, device=dev)
         if fp8:
             w13 = torch.empty((G, 2 * I, d), dtype=torch.uint8, device=dev)
             w2 = torch.empty((G, d, I), dtype=torch.uint8, device=dev)
@@ -67,13 +77,19 @@ class MoELayer:
         for e in range(G):
             w1, w3, w2e = expert_weights(e)
             w13e = interleave_gate_up(w1, w3)
+            if train:
+                w13m[e].copy_(w13e)
+                w2m[e].copy_(w2e)
             if fp8:
                 fp8_quant_128x128(w13e, w13[e], s13[e])
                 fp8_quant_128x128(w2e.contiguous(), w2[e], s2[e])
             else:
                 w13[e].copy_(w13e)
                 w2[e].copy_(w2e)
-        return cls(d, N, K, I, centroids, bias, w13, w2, s13, s2, **kw)
+        layer = cls(d, N, K, I, centroids, bias, w13, w2, s13, s2, **kw)
+        if train:
+            layer.enable_training(w13m, w2m)
+        return layer
 
     def prepare_centroids(self):
         """Re-prepares the gate's operand; call after changing self.centroids in place."""
@@ -160,6 +176,100 @@ class MoELayer:
             ctypes.byref(outs), int(update_bias), int(slot), _p(ws), ws.numel(), _stream(),
             ctypes.c_void_p(done.cuda_event)), "moe_layer_forward_host_pipelined")
         return out_host
+
+    # ------------------------------------------------------------------
+    # training
+    # ------------------------------------------------------------------
+
+    def enable_training(self, w13_master: torch.Tensor, w2_master: torch.Tensor):
+        """fp32 masters [N+1, 2I, d] (W13's interleaved rows) and [N+1, d, I]
+        whose 128x128 quantisation the layer's FP8 weights are; allocates the
+        transposed FP8 weights and the gradients."""
+        if not self.fp8:
+            raise ValueError("training needs a FP8 layer")
+        dev, G, d, I, N = self.centroids.device, self.N + 1, self.d, self.I, self.N
+        self.w13_master, self.w2_master = w13_master, w2_master
+        self.w13t, self.w13t_scales = fp8_transpose_128x128(self.w13, self.w13_scales)
+        self.w2t, self.w2t_scales = fp8_transpose_128x128(self.w2, self.w2_scales)
+        self.dw13 = torch.empty((G, 2 * I, d), dtype=torch.float32, device=dev)
+        self.dw2 = torch.empty((G, d, I), dtype=torch.float32, device=dev)
+        self.dcentroids = torch.empty((N, d), dtype=torch.float32, device=dev)
+        self._wt = LayerWeightsT(w13t=self.w13t.data_ptr(), w13t_scales=self.w13t_scales.data_ptr(),
+                                 w2t=self.w2t.data_ptr(), w2t_scales=self.w2t_scales.data_ptr())
+        self._masters = LayerMasters(w13=w13_master.data_ptr(), w2=w2_master.data_ptr())
+        self._train_ws = {}
+
+    def train_workspace(self, T: int) -> torch.Tensor:
+        ws = self._train_ws.get(T)
+        if ws is None:
+            need = load_library().moe_layer_train_workspace_size(ctypes.byref(self._desc), T)
+            ws = torch.empty((max(int(need), 1),), dtype=torch.uint8, device=self.centroids.device)
+            self._train_ws[T] = ws
+        return ws
+
+    def train_buffer(self, T: int, name: str) -> torch.Tensor:
+        """A named buffer of the training workspace for T tokens (after
+        forward_train / backward): H, scores, dg, dA, dH, dX, offsets,
+        perm_token, dest_row, y, kofs, dy_q, dy_s, dh_q, dh_s, row_gate."""
+        off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+        _check(load_library().moe_layer_train_buffer(ctypes.byref(self._desc), T, TRAIN_BUFFERS[name],
+                                                     ctypes.byref(off), ctypes.byref(nb)), "moe_layer_train_buffer")
+        raw = self.train_workspace(T)[off.value:off.value + nb.value]
+        R, d, I, N, K = T * self.K + T, self.d, self.I, self.N, self.K
+        shape, dtype = {
+            "H": ((R, 2 * I), torch.bfloat16), "scores": ((T, N), torch.float32), "dg": ((T, K), torch.float32),
+            "dA": ((R, I), torch.bfloat16), "dH": ((R, 2 * I), torch.bfloat16), "dX": ((R, d), torch.bfloat16),
+            "offsets": ((N + 2,), torch.int32), "perm_token": ((T * K,), torch.int32),
+            "dest_row": ((T, K), torch.int32), "y": ((R, d), torch.bfloat16), "kofs": ((N + 2,), torch.int32),
+            "dy_q": ((R, d), torch.uint8), "dy_s": ((d // 128, R), torch.float32),
+            "dh_q": ((R, 2 * I), torch.uint8), "dh_s": ((2 * I // 128, R), torch.float32),
+            "row_gate": ((R,), torch.float32),
+        }[name]
+        return raw.view(dtype).view(shape)
+
+    def _grads(self, dz):
+        return LayerGrads(dw13=self.dw13.data_ptr(), dw2=self.dw2.data_ptr(), dcentroids=self.dcentroids.data_ptr(),
+                          dz=dz.data_ptr() if dz is not None else None)
+
+    def forward_train(self, u: torch.Tensor, out: torch.Tensor = None, update_bias: bool = True, topk_idx=None,
+                      gates=None) -> torch.Tensor:
+        """forward that keeps what the backward reads (in the training workspace)."""
+        T = u.shape[0]
+        out = torch.empty_like(u) if out is None else out
+        ws = self.train_workspace(T)
+        outs = self._outs(topk_idx, gates)
+        _check(load_library().moe_layer_forward_train(ctypes.byref(self._desc), _p(u), T, _p(out),
+                                                      ctypes.byref(outs), int(update_bias), _p(ws), ws.numel(),
+                                                      _stream()), "moe_layer_forward_train")
+        return out
+
+    def backward(self, u: torch.Tensor, dout: torch.Tensor, du: torch.Tensor = None, dz: torch.Tensor = None):
+        """Gradients of the last forward_train on u: dout = dL/dh' bf16 [T, d] ->
+        du bf16 [T, d]; dw13, dw2, dcentroids (and dz [T, K] if given) filled."""
+        T = u.shape[0]
+        du = torch.empty_like(u) if du is None else du
+        ws = self.train_workspace(T)
+        grads = self._grads(dz)
+        _check(load_library().moe_layer_backward(ctypes.byref(self._desc), ctypes.byref(self._wt), _p(u), T,
+                                                 _p(dout), _p(du), ctypes.byref(grads), _p(ws), ws.numel(),
+                                                 _stream()), "moe_layer_backward")
+        return du
+
+    def train_step(self, u: torch.Tensor, dout: torch.Tensor, lr: float, out: torch.Tensor = None,
+                   du: torch.Tensor = None):
+        """One SGD step (forward_train with the bias update, backward, SGD on the
+        masters and the fp32 centroids, FP8 weights quantised again) -> (h', du)."""
+        T = u.shape[0]
+        out = torch.empty_like(u) if out is None else out
+        du = torch.empty_like(u) if du is None else du
+        ws = self.train_workspace(T)
+        outs = self._outs(None, None)
+        grads = self._grads(None)
+        _check(load_library().moe_layer_train_step(ctypes.byref(self._desc), ctypes.byref(self._wt),
+                                                   ctypes.byref(self._masters), _p(u), T, _p(dout), float(lr),
+                                                   _p(out), _p(du), ctypes.byref(outs), ctypes.byref(grads), _p(ws),
+                                                   ws.numel(), _stream()), "moe_layer_train_step")
+        return out, du
 
 
 class LayerGraph:

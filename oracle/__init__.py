@@ -482,8 +482,11 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
 
     fp8=True follows the FP8 path's storage and quantisation points: the
     forward keeps H = X W13^T (FP8 product) rounded to bf16 and its expert
-    outputs y in bf16; dY is formed in fp32 and quantised per 1x128 tile for
-    dA = dY W2 (W2's forward 128x128 blocks, transposed), dA is stored in bf16;
+    outputs y in bf16; dY = g G_t is quantised per 1x128 tile for dA = dY W2
+    (W2's forward 128x128 blocks, transposed) -- the tile rule is
+    scale-invariant, so that is G_t's codes with g times G_t's scales
+    (fl32(g s)) -- and dA is stored in bf16; for the weight gradient dY is
+    formed in fp32 (fl32(g G));
     dH is computed from the stored H and dA and stored in bf16, quantised per
     1x128 tile for dX = dH W13 (bf16 out); the weight gradients quantise both
     operands per (128 rows of the expert, column) -- dY, A recomputed in fp32
@@ -548,7 +551,9 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
             Y = _bf(fp8_gemm(aq, as_, q2, s2))
             Ht1, Ht3 = _bf(H1), _bf(H3)
             dY = _r32(gr[:, None] * Gv[toks])
-            qy, sy = quant_1x128_f32(dY)
+            # the 1x128 rule on g G_t: scale-invariant, so G_t's codes and g times its scales
+            qy, sg = quant_1x128(as_bf16_bits(G_bf16)[toks])
+            sy = _r32(gr[:, None] * sg.astype(np.float64))
             dA = _bf(fp8_gemm(qy, sy, q2.T, s2.T))
             dH1, dH3 = swiglu_backward(Ht1, Ht3, dA)
             dHt1, dHt3 = _bf(dH1), _bf(dH3)
@@ -603,6 +608,12 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
     return out
 
 
+def sgd_f32(w, grad, lr) -> np.ndarray:
+    """Plain SGD on an fp32 master: fl32(w - fl32(lr * fl32(grad)))."""
+    step = (np.float32(lr) * _r32(grad)).astype(np.float32)
+    return (np.asarray(w, np.float32) - step).astype(np.float32)
+
+
 def train_step(u_bf16, masters: dict, bias: np.ndarray, K: int, G_bf16, lr: float, gamma: float, n_groups=1,
                topk_groups=1):
     """One training step of the layer (readings in moe_oracle.c, [train], [bias]):
@@ -615,11 +626,7 @@ def train_step(u_bf16, masters: dict, bias: np.ndarray, K: int, G_bf16, lr: floa
     m = {k: np.asarray(v, np.float32) for k, v in masters.items()}
     bw = layer_backward(u_bf16, m["e"], bias, K, lambda e: (m["w1"][e], m["w3"][e], m["w2"][e]), G_bf16,
                         n_groups=n_groups, topk_groups=topk_groups, fp8=True)
-    lr32 = np.float32(lr)
-    new = {}
-    for k, grad in (("w1", bw.dw1), ("w3", bw.dw3), ("w2", bw.dw2), ("e", bw.de)):
-        step = (lr32 * _r32(grad)).astype(np.float32)
-        new[k] = (m[k] - step).astype(np.float32)
+    new = {k: sgd_f32(m[k], grad, lr) for k, grad in (("w1", bw.dw1), ("w3", bw.dw3), ("w2", bw.dw2), ("e", bw.de))}
     T = as_bf16_bits(u_bf16).shape[0]
     new_bias = bias_update(bias, bw.route.loads, T, K, gamma)
     return new, new_bias, bw

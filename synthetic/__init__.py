@@ -212,6 +212,11 @@ def tokens(shape: LayerShape, seed: int = 0, device="cpu", start_token: int = 0,
                   start=start_token * shape.d)
 
 
+def grad_out(shape: LayerShape, seed: int = 0, device="cpu", std: float = 1.0) -> torch.Tensor:
+    """An incoming gradient dL/dh' ~ N(0, std^2) bf16 [T, d] for the backward pass."""
+    return normal((shape.T, shape.d), std, key(seed, "grad-out", shape.d), device)
+
+
 def bias(shape: LayerShape, seed: int = 0, zero: bool = False, device="cpu") -> torch.Tensor:
     if zero:
         return torch.zeros(shape.N, dtype=torch.float32, device=device)

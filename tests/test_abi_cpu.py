@@ -195,3 +195,71 @@ def test_balance_stats_checks_its_arguments(L):
     assert need >= 8 * 2 * 64 * 8                              # 8 sequences x 2 chunks x 64 experts x 8 bytes
     assert call(1000, 64, 8, 128, need - 1) == M.MOE_ERR_WORKSPACE
     assert call(0, 64, 8, 128, 0) == M.MOE_OK                  # no tokens: nothing to do
+
+
+def _layer_desc(fp8=1, I=256, d=256, N=8, K=2):
+    p = 4096
+    return M.LayerWeights(d=d, N=N, K=K, I=I, n_groups=1, topk_groups=1, gamma=1e-3, fp8=fp8, centroids=p,
+                          centroid_dtype=M.MOE_DTYPE_F32, bias=p, w13=p, w13_scales=p, w2=p, w2_scales=p,
+                          centroids_prepared=None)
+
+
+def test_training_entry_points_check_their_arguments(L):
+    p, s = _ok_ptr(), ctypes.c_void_p(0)
+    w = _layer_desc()
+    # workspace: the forward's plus H, the affinities and the backward's buffers
+    T = 100
+    fwd, tr = L.moe_layer_workspace_size(ctypes.byref(w), T), L.moe_layer_train_workspace_size(ctypes.byref(w), T)
+    R = T * w.K + T
+    assert tr > fwd + R * 2 * w.I * 2 + T * w.N * 4
+    # named buffers lie inside the workspace and do not overlap
+    spans = []
+    for name, which in M.TRAIN_BUFFERS.items():
+        off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+        assert L.moe_layer_train_buffer(ctypes.byref(w), T, which, ctypes.byref(off), ctypes.byref(nb)) == M.MOE_OK
+        assert off.value % 256 == 0 and off.value + nb.value <= tr, name
+        spans.append((off.value, off.value + nb.value, name))
+    spans.sort()
+    for a, b in zip(spans, spans[1:]):
+        assert a[1] <= b[0], (a, b)
+    off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert L.moe_layer_train_buffer(ctypes.byref(w), T, 99, ctypes.byref(off), ctypes.byref(nb)) \
+        == M.MOE_ERR_INVALID_ARG
+    # bf16 layers and I not a multiple of 256 are refused
+    outs = M.LayerOutputs(topk_idx=None, gates=None, loads=4096, stage_events=None)
+    wb = _layer_desc(fp8=0)
+    assert L.moe_layer_forward_train(ctypes.byref(wb), p, T, p, ctypes.byref(outs), 1, p, 1 << 40, s) \
+        == M.MOE_ERR_UNSUPPORTED
+    wi = _layer_desc(I=384)
+    assert L.moe_layer_forward_train(ctypes.byref(wi), p, T, p, ctypes.byref(outs), 1, p, 1 << 40, s) \
+        == M.MOE_ERR_INVALID_ARG
+    # a too-small workspace
+    assert L.moe_layer_forward_train(ctypes.byref(w), p, T, p, ctypes.byref(outs), 1, p, tr - 1, s) \
+        == M.MOE_ERR_WORKSPACE
+    # the backward needs the transposed weights and every gradient buffer
+    wt = M.LayerWeightsT(w13t=4096, w13t_scales=4096, w2t=4096, w2t_scales=4096)
+    g_missing = M.LayerGrads(dw13=4096, dw2=None, dcentroids=4096, dz=None)
+    assert L.moe_layer_backward(ctypes.byref(w), ctypes.byref(wt), p, T, p, p, ctypes.byref(g_missing), p, tr, s) \
+        == M.MOE_ERR_INVALID_ARG
+    wt0 = M.LayerWeightsT(w13t=None, w13t_scales=4096, w2t=4096, w2t_scales=4096)
+    g = M.LayerGrads(dw13=4096, dw2=4096, dcentroids=4096, dz=None)
+    assert L.moe_layer_backward(ctypes.byref(w), ctypes.byref(wt0), p, T, p, p, ctypes.byref(g), p, tr, s) \
+        == M.MOE_ERR_INVALID_ARG
+    # the training step needs fp32 centroids and masters
+    m = M.LayerMasters(w13=None, w2=4096)
+    assert L.moe_layer_train_step(ctypes.byref(w), ctypes.byref(wt), ctypes.byref(m), p, T, p, 0.1, p, p,
+                                  ctypes.byref(outs), ctypes.byref(g), p, tr, s) == M.MOE_ERR_INVALID_ARG
+    wc = _layer_desc()
+    wc.centroid_dtype = M.MOE_DTYPE_BF16
+    m = M.LayerMasters(w13=4096, w2=4096)
+    assert L.moe_layer_train_step(ctypes.byref(wc), ctypes.byref(wt), ctypes.byref(m), p, T, p, 0.1, p, p,
+                                  ctypes.byref(outs), ctypes.byref(g), p, tr, s) == M.MOE_ERR_UNSUPPORTED
+    # weight-gradient GEMM, transpose and SGD shape rules
+    assert L.fp8_grouped_gemm_wgrad(p, p, p, p, p, 4, 100, 256, 256, p, s) == M.MOE_ERR_INVALID_ARG
+    assert L.fp8_grouped_gemm_wgrad(p, p, p, p, p, 4, 128, 128, 256, p, s) == M.MOE_ERR_INVALID_ARG
+    assert L.fp8_grouped_gemm_wgrad(p, p, p, p, p, 4, 128, 256, 200, p, s) == M.MOE_ERR_INVALID_ARG
+    assert L.fp8_grouped_gemm_wgrad(p, p, p, p, p, 2000, 128, 256, 256, p, s) == M.MOE_ERR_INVALID_ARG
+    assert L.fp8_transpose_128x128(p, p, 1, 100, 128, p, p, s) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_sgd_requant_128x128(p, p, 1, 128, 96, 0.1, p, p, p, p, s) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_sgd_f32(p, p, -1, 0.1, s) == M.MOE_ERR_INVALID_ARG
+    assert L.moe_sgd_f32(None, None, 0, 0.1, s) == M.MOE_OK
