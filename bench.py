@@ -611,6 +611,114 @@ def case_decode(moe, S, dev, args, flush, v3_layer, dsh, cpu_baseline=True):
     return res
 
 
+def case_train(moe, S, dev, args, flush, cpu_baseline=True):
+    """One training step of the V3 layer (T=8192, d=7168, 256 routed + 1
+    shared experts, top-8, I=2048): the training forward (keeps the affinities
+    and GEMM 1's products), the backward (FP8 products for dA, dX and both
+    weight gradients on the tensor cores; combine, SwiGLU and gate backward),
+    and SGD on the fp32 masters with the FP8 weights quantised again."""
+    import numpy as np
+    import torch
+
+    import oracle
+    sh = S.LAYER_V3
+    T, d, N, K, I = sh.T, sh.d, sh.N, sh.K, sh.I
+    G_ = N + 1
+    R = T * K + T
+    pk, src = peaks()
+    cent = S.centroids(sh, zipf=True).to(dev)
+    bias = S.bias(sh).to(dev)
+    layer = moe.MoELayer.build(d, N, K, I, cent, bias, lambda e: S.expert_weights(sh, e, device=dev), fp8=True,
+                               train=True, gamma=sh.gamma)
+    u = S.tokens(sh, seed=5, device=dev)
+    G = S.grad_out(sh, seed=5, device=dev)
+    out, du = torch.empty_like(u), torch.empty_like(u)
+    ms_fwd = time_launches(lambda: layer.forward_train(u, out, update_bias=False), args.steps, args.warmup, flush)
+    # the backward, its stages timed by events on the launching stream
+    names = ["combine_bwd", "gemm_dA", "swiglu_bwd", "gemm_dX", "gates_du_centroids", "wgrad_operands",
+             "gemm_dW2", "gemm_dW13"]
+    for _ in range(args.warmup):
+        flush()
+        layer.backward(u, G, du)
+    torch.cuda.synchronize()
+    runs = []
+    for _ in range(args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        flush()
+        layer.backward(u, G, du, stage_events=ev)
+        runs.append(ev)
+    torch.cuda.synchronize()
+    stage = {n: statistics.mean(r[i].elapsed_time(r[i + 1]) for r in runs) for i, n in enumerate(names)}
+    ms_bwd = statistics.mean(r[0].elapsed_time(r[-1]) for r in runs)
+    assert moe.device_status() == 0
+    # the SGD step on both masters with their re-quantisation (two launches), alone
+    def sgd():
+        moe.moe_sgd_requant_128x128(layer.w13_master, layer.dw13, 1e-7, layer.w13, layer.w13_scales, layer.w13t,
+                                    layer.w13t_scales)
+        moe.moe_sgd_requant_128x128(layer.w2_master, layer.dw2, 1e-7, layer.w2, layer.w2_scales, layer.w2t,
+                                    layer.w2t_scales)
+    ms_sgd = time_launches(sgd, args.steps, args.warmup, flush)
+    ms_step = time_launches(lambda: layer.train_step(u, G, 1e-7, out, du), args.steps, args.warmup, flush)
+    assert moe.device_status() == 0
+    # rooflines: the backward's two weight-gradient GEMMs write fp32 [G, M, Nd]
+    # gradients; their operands are read once from HBM (re-reads hit L2)
+    Kp = ((R + 127) // 128 + G_) * 128
+    n_w = G_ * 3 * I * d                                     # parameters of the experts
+    rl = {
+        "gemm_dA": ("tensor", 2.0 * R * d * I),
+        "gemm_dX": ("tensor", 2.0 * R * d * 2 * I),
+        "gemm_dW2": ("hbm", G_ * d * I * 4 + (d + I) * Kp + (d + I) * Kp // 32),
+        "gemm_dW13": ("hbm", G_ * 2 * I * d * 4 + (2 * I + d) * Kp + (2 * I + d) * Kp // 32),
+        "combine_bwd": ("hbm", T * d * 2 + T * K * d * 2 + R * d + R * d // 32),
+        "swiglu_bwd": ("hbm", R * I * 2 + R * 2 * I * 2 * 2 + R * 2 * I + R * 2 * I // 32),
+        "gates_du_centroids": ("hbm", T * d * 2 * 2 + R * d * 2 + T * K * d * 2),
+        "wgrad_operands": ("hbm", R * (d + 2 * I + 2 * I + d) * 2 + Kp * (2 * d + 3 * I) * 1),
+    }
+    fp8_peak, fp8_src = fp8_peak_tflops(pk, ms_bwd * args.steps / 1e3)
+    roof = {}
+    for n, (bound, amount) in rl.items():
+        if bound == "tensor":
+            a = amount / (stage[n] * 1e-3) / 1e12
+            roof[n] = {"bound": "tensor", "achieved": a, "peak": fp8_peak, "unit": "TFLOP/s", "frac": a / fp8_peak}
+        else:
+            a = amount / (stage[n] * 1e-3) / 1e9
+            roof[n] = {"bound": "hbm", "achieved": a, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                       "frac": a / pk["hbm_gbs"]}
+    sgd_bytes = n_w * (4 + 4 + 4 + 1 + 1) + n_w // 16384 * 8
+    sgd_gbs = sgd_bytes / (ms_sgd * 1e-3) / 1e9
+    top = max(stage, key=stage.get)
+    res = {"workload": "train-step-v3-8192x7168-256e-top8-I2048", "ms": ms_step, "tokens_per_s": T / ms_step * 1e3,
+           "ms_forward_train": ms_fwd, "ms_backward": ms_bwd, "ms_sgd_requant": ms_sgd,
+           "backward_stages_ms": stage, "backward_rooflines": roof,
+           "sgd_requant": {"bound": "hbm", "achieved": sgd_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": sgd_gbs / pk["hbm_gbs"], "bytes": sgd_bytes,
+                           "note": "reads the fp32 master and gradient, writes the master, the E4M3 codes "
+                                   "and their transposed copy"},
+           "roofline": dict(roof[top], kernel=f"backward stage {top}", traffic=None,
+                            peak_source=f"{src} ({fp8_src})" if roof[top]["bound"] == "tensor" else f"{src} hbm copy"),
+           "lr": 1e-7, "l2": "flushed before each step",
+           "note": "step = training forward + backward + SGD with re-quantisation of every expert weight; "
+                   "at this batch the SGD over 11.3 G parameters (fp32 master and gradient) dominates"}
+    if cpu_baseline:
+        n = 2
+        toks = torch.arange(n)
+        uh, Gh = u[:n].cpu(), G[:n].cpu()
+        r = oracle.route(uh, cent.cpu(), bias.cpu(), K, want_scores=True)
+        cache = {e: tuple(w.cpu() for w in S.expert_weights(sh, e, device=dev))
+                 for e in sorted(set(r.topk_idx.ravel().tolist()) | {N})}
+        t0 = time.perf_counter()
+        oracle.layer_backward(uh, cent.cpu(), bias.cpu().numpy(), K, lambda e: cache[e], Gh, fp8=True, route_all=r,
+                              stack=False)
+        dt = time.perf_counter() - t0
+        res["cpu_baseline"] = _cpu(n / dt, "tokens/s", oracle.threads(),
+                                   f"{n} tokens: the FP8 forward and backward through their {len(cache)} experts "
+                                   f"(weight quantisation, products, weight gradients over 128 padded rows), "
+                                   f"without the SGD ({dt:.1f} s)")
+    del layer
+    torch.cuda.empty_cache()
+    return res
+
+
 def case_dispatch(moe, S, dev, args, flush, which):
     """The V3 layer's dispatch (permute with 1x128 E4M3 quantisation and the shared
     expert's rows, `permute-fp8`) or combine (`combine`) alone, T = 8192, d = 7168,
@@ -703,6 +811,8 @@ def run_case(args):
         line.update(case_tiny(moe, S, dev, args, flush, cpu_baseline=cb))
     elif args.case in ("permute-fp8", "combine"):
         line.update(case_dispatch(moe, S, dev, args, flush, args.case))
+    elif args.case == "train":
+        line.update(case_train(moe, S, dev, args, flush, cpu_baseline=cb))
     elif args.case in ("decode64", "decode256"):
         sh = S.LAYER_V3
         cent = S.centroids(sh, zipf=True).to(dev)
@@ -725,7 +835,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="time the V3 layer only")
     ap.add_argument("--case", default="layer",
                     choices=["layer", "tiny", "route", "gemm", "gemm1-small", "gemm2-small", "decode64",
-                             "decode256", "permute-fp8", "combine"],
+                             "decode256", "permute-fp8", "combine", "train"],
                     help="layer: the V3 layer step with every other workload (the benchmark line); the others "
                          "time one workload alone")
     args = ap.parse_args()

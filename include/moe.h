@@ -382,7 +382,14 @@ typedef struct {
     float* dw2;                /* [N+1][d][I] fp32; required */
     float* dcentroids;         /* [N][d] fp32; required */
     float* dz;                 /* [T, K] fp32 gradient of the chosen experts' logits; optional */
+    /* NULL, or MOE_BACKWARD_STAGES + 1 cudaEvent_t recorded on `stream` before
+     * the first stage and after each stage of moe_layer_backward (combine
+     * backward, GEMM dA, SwiGLU backward, GEMM dX, gates + du + centroid
+     * gradient, weight-gradient operands, GEMM dW2, GEMM dW13). */
+    void* const* stage_events;
 } moe_layer_grads;
+
+#define MOE_BACKWARD_STAGES 8
 
 /* fp32 master copies of the FP8 layer's expert weights (training step). */
 typedef struct {

@@ -65,7 +65,10 @@ class LayerWeightsT(ctypes.Structure):
 
 class LayerGrads(ctypes.Structure):
     _fields_ = [("dw13", ctypes.c_void_p), ("dw2", ctypes.c_void_p), ("dcentroids", ctypes.c_void_p),
-                ("dz", ctypes.c_void_p)]
+                ("dz", ctypes.c_void_p), ("stage_events", ctypes.c_void_p)]
+
+
+BACKWARD_STAGES = 8
 
 
 class LayerMasters(ctypes.Structure):

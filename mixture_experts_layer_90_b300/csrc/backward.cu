@@ -434,58 +434,52 @@ __global__ void __launch_bounds__(256) fp8_transpose_kernel(const uint8_t* __res
 // One block per (group, 128x128 block) of an fp32 master [G][rows][cols]:
 // w <- fl32(w - fl32(lr * grad)), then the block's scale amax/448 and codes,
 // stored row-major (q, s [G][rows/128][cols/128]) and transposed (qt [G][cols][rows],
-// st [G][cols/128][rows/128]). Thread t: row t/2, 64 columns.
+// st [G][cols/128][rows/128]). Warp w takes rows 16w..16w+15 of the block and
+// lane l columns 4l..4l+3, so every load and store of a warp covers one whole
+// 512-byte row of the block.
 __global__ void __launch_bounds__(256) sgd_requant_kernel(float* __restrict__ w, const float* __restrict__ grad,
                                                           int rows, int cols, float lr, uint8_t* __restrict__ q,
                                                           float* __restrict__ s, uint8_t* __restrict__ qt,
                                                           float* __restrict__ st) {
-    __shared__ uint8_t tile[128][129];
+    __shared__ uint8_t tile[128][132];
     __shared__ float warp_max[8];
     const int bc = blockIdx.x, br = blockIdx.y;
     const int64_t g = blockIdx.z;
-    const int tid = threadIdx.x;
-    const int r = tid >> 1, cbase = (tid & 1) * 64;
-    const int64_t off = g * int64_t(rows) * cols + int64_t(br * 128 + r) * cols + bc * 128 + cbase;
-    float4* wp = reinterpret_cast<float4*>(w + off);
-    const float4* gp = reinterpret_cast<const float4*>(grad + off);
+    const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+    const int64_t base = g * int64_t(rows) * cols + int64_t(br * 128 + 16 * wp) * cols + bc * 128 + 4 * lane;
+    float4 x[16];
     float amax = 0.0f;
-#pragma unroll 4
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
-        float4 x = wp[i];
-        const float4 d = __ldg(gp + i);
+        const int64_t off = base + int64_t(i) * cols;
+        float4 v = *reinterpret_cast<const float4*>(w + off);
+        const float4 d = __ldg(reinterpret_cast<const float4*>(grad + off));
         // two fp32 roundings, never fused: the product, then the difference
-        x.x = __fsub_rn(x.x, __fmul_rn(lr, d.x));
-        x.y = __fsub_rn(x.y, __fmul_rn(lr, d.y));
-        x.z = __fsub_rn(x.z, __fmul_rn(lr, d.z));
-        x.w = __fsub_rn(x.w, __fmul_rn(lr, d.w));
-        wp[i] = x;
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+        v.x = __fsub_rn(v.x, __fmul_rn(lr, d.x));
+        v.y = __fsub_rn(v.y, __fmul_rn(lr, d.y));
+        v.z = __fsub_rn(v.z, __fmul_rn(lr, d.z));
+        v.w = __fsub_rn(v.w, __fmul_rn(lr, d.w));
+        *reinterpret_cast<float4*>(w + off) = v;
+        x[i] = v;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if ((tid & 31) == 0) warp_max[tid >> 5] = amax;
+    if (lane == 0) warp_max[wp] = amax;
     __syncthreads();
     amax = warp_max[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
     const float sc = tile_scale(amax);
-    uint8_t* qrow = q + off;
-#pragma unroll 2
-    for (int i = 0; i < 16; i += 2) {
-        const float4 x0 = wp[i], x1 = wp[i + 1];   // this thread's own stores, read back
-        const uint32_t a0 = pack_e4m3x2(__fdiv_rn(x0.x, sc), __fdiv_rn(x0.y, sc)) |
-                            (pack_e4m3x2(__fdiv_rn(x0.z, sc), __fdiv_rn(x0.w, sc)) << 16);
-        const uint32_t a1 = pack_e4m3x2(__fdiv_rn(x1.x, sc), __fdiv_rn(x1.y, sc)) |
-                            (pack_e4m3x2(__fdiv_rn(x1.z, sc), __fdiv_rn(x1.w, sc)) << 16);
-        reinterpret_cast<uint2*>(qrow)[i / 2] = make_uint2(a0, a1);
-        const int cc = cbase + 4 * i;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            tile[r][cc + j] = uint8_t(a0 >> (8 * j));
-            tile[r][cc + 4 + j] = uint8_t(a1 >> (8 * j));
-        }
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t c = pack_e4m3x2(__fdiv_rn(x[i].x, sc), __fdiv_rn(x[i].y, sc)) |
+                           (pack_e4m3x2(__fdiv_rn(x[i].z, sc), __fdiv_rn(x[i].w, sc)) << 16);
+        *reinterpret_cast<uint32_t*>(q + base + int64_t(i) * cols) = c;
+        *reinterpret_cast<uint32_t*>(&tile[16 * wp + i][4 * lane]) = c;
     }
     __syncthreads();
+    // transposed: 8 lanes per output row of 128 bytes (16 each), 32 rows per pass
     uint8_t* dst = qt + g * int64_t(rows) * cols;
     for (int c = tid >> 3; c < 128; c += 32) {
         uint4 v;

@@ -646,6 +646,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         st_global_32B(reinterpret_cast<uint16_t*>(args.C) + (int64_t(s.offs[it.g]) + rl) * args.Nd + c0,
                                       w + 8 * i);
                 }
+            } else if (kW) {
+                // weight gradient, fp32 [G][M][Nd]: per 32-column half, four lanes swap
+                // 32-byte pieces (a 4x4 transpose by two xor-shuffle rounds), so that in
+                // store i the lanes 4a..4a+3 write the 128 bytes of row 4a+i: every store
+                // instruction of the warp writes 8 whole 128-byte lines
+                const bool b0 = lane & 1, b1 = lane & 2;
+                const int64_t rbase = int64_t(it.g) * args.M_total + it.mt * kBM + q * 32 + (lane & ~3);
+                float* cbase = reinterpret_cast<float*>(args.C) + int64_t(it.nt) * kBN + slice + 8 * (lane & 3);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float* x = acc + 32 * half;   // swapped in place
+#pragma unroll
+                    for (int c = 0; c < 4; c += 2)
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const float v = __shfl_xor_sync(0xffffffffu, b0 ? x[8 * c + r] : x[8 * c + 8 + r], 1);
+                            if (b0) x[8 * c + r] = v;
+                            else x[8 * c + 8 + r] = v;
+                        }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const float v = __shfl_xor_sync(0xffffffffu, b1 ? x[8 * c + r] : x[8 * c + 16 + r], 2);
+                            if (b1) x[8 * c + r] = v;
+                            else x[8 * c + 16 + r] = v;
+                        }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) w[j] = __float_as_uint(x[8 * i + j]);
+                        st_global_32B(cbase + (rbase + i) * args.Nd + 32 * half, w);
+                    }
+                }
             } else if (valid) {
                 // MOE_EPI_F32: split-K partial sums, [splits][M_total][Nd]
                 const int64_t c0 = int64_t(it.nt) * kBN + slice;

@@ -98,6 +98,9 @@ moe_status layer_backward(const moe_layer_weights* w, const moe_layer_weights_t*
     const int K = w->K, N = w->N, d = w->d, I = w->I, G = N + 1;
     const int64_t R = T * K + T;
     if (T == 0) {
+        if (gr->stage_events)
+            for (int i = 0; i <= MOE_BACKWARD_STAGES; ++i)
+                CUDA_OK(cudaEventRecord(reinterpret_cast<cudaEvent_t>(gr->stage_events[i]), stream));
         // no token: every gradient is zero
         CUDA_OK(cudaMemsetAsync(gr->dw13, 0, size_t(G) * 2 * I * d * 4, stream));
         CUDA_OK(cudaMemsetAsync(gr->dw2, 0, size_t(G) * d * I * 4, stream));
@@ -124,21 +127,31 @@ moe_status layer_backward(const moe_layer_weights* w, const moe_layer_weights_t*
     uint16_t* dX = reinterpret_cast<uint16_t*>(ws + W.dX);
     int32_t* kofs = reinterpret_cast<int32_t*>(ws + W.kofs);
     float* dz_row = reinterpret_cast<float*>(ws + W.dz_row);
+    auto mark = [&](int i) -> moe_status {
+        if (gr->stage_events) CUDA_OK(cudaEventRecord(reinterpret_cast<cudaEvent_t>(gr->stage_events[i]), stream));
+        return MOE_OK;
+    };
 
+    STATUS_OK(mark(0));
     // combine backward: dg and the dgrad operand dY (1x128 tiles)
     CUDA_OK(moe::launch_combine_bwd(dout, y, gates, dest, T, d, K, R, qdy, sdy, row_gate, dg, stream));
+    STATUS_OK(mark(1));
     // dA = dY W2 (W2's blocks transposed), bf16
     STATUS_OK(fp8_gemm_impl(qdy, sdy, wt->w2t, wt->w2t_scales, offsets, G, R, I, d, MOE_EPI_BF16, dA, nullptr,
                             nullptr, stream));
+    STATUS_OK(mark(2));
     // dH from H and dA, bf16 and 1x128 tiles
     CUDA_OK(moe::launch_swiglu_bwd(dA, H, R, I, dH, qdh, sdh, stream));
+    STATUS_OK(mark(3));
     // dX = dH W13 (W13's blocks transposed), bf16
     STATUS_OK(fp8_gemm_impl(qdh, sdh, wt->w13t, wt->w13t_scales, offsets, G, R, d, 2 * I, MOE_EPI_BF16, dX,
                             nullptr, nullptr, stream));
+    STATUS_OK(mark(4));
     // gates and du
     CUDA_OK(moe::launch_unpermute_bwd(dout, dX, dest, topk, gates, scores, dg, w->centroids,
                                       w->centroid_dtype == MOE_DTYPE_F32, T, d, N, K, du, dz_row, gr->dz, stream));
     CUDA_OK(moe::launch_centroid_grad(u, offsets, perm_token, dz_row, N, d, gr->dcentroids, stream));
+    STATUS_OK(mark(5));
     // weight gradients: operands per (128 tokens of an expert, column), transposed
     CUDA_OK(moe::launch_kblock_offsets(offsets, G, kofs, stream));
     const int64_t Kp = W.Kp, TK = T * K;
@@ -158,9 +171,12 @@ moe_status layer_backward(const moe_layer_weights* w, const moe_layer_weights_t*
                                 stream));
     CUDA_OK(moe::launch_quant_t(moe::kQuantTTokens, offsets, kofs, G, TK, perm_token, nullptr, u, d, Kp, qxt, sxt,
                                 stream));
+    STATUS_OK(mark(6));
     // dW2 = dY^T A  [G][d][I];  dW13 = dH^T X  [G][2I][d]
     STATUS_OK(wgrad_gemm(qyt, syt, qat, sat, kofs, G, d, I, Kp, gr->dw2, stream));
+    STATUS_OK(mark(7));
     STATUS_OK(wgrad_gemm(qht, sht, qxt, sxt, kofs, G, 2 * I, d, Kp, gr->dw13, stream));
+    STATUS_OK(mark(8));
     return MOE_OK;
 }
 

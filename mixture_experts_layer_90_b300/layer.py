@@ -227,9 +227,16 @@ class MoELayer:
         }[name]
         return raw.view(dtype).view(shape)
 
-    def _grads(self, dz):
+    def _grads(self, dz, events=None):
+        self._bwd_ev = None
+        if events is not None:
+            for e in events:
+                if e.cuda_event == 0:      # torch creates the CUDA event on its first record
+                    e.record()
+            self._bwd_ev = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         return LayerGrads(dw13=self.dw13.data_ptr(), dw2=self.dw2.data_ptr(), dcentroids=self.dcentroids.data_ptr(),
-                          dz=dz.data_ptr() if dz is not None else None)
+                          dz=dz.data_ptr() if dz is not None else None,
+                          stage_events=ctypes.cast(self._bwd_ev, ctypes.c_void_p) if events is not None else None)
 
     def forward_train(self, u: torch.Tensor, out: torch.Tensor = None, update_bias: bool = True, topk_idx=None,
                       gates=None) -> torch.Tensor:
@@ -243,13 +250,16 @@ class MoELayer:
                                                       _stream()), "moe_layer_forward_train")
         return out
 
-    def backward(self, u: torch.Tensor, dout: torch.Tensor, du: torch.Tensor = None, dz: torch.Tensor = None):
+    def backward(self, u: torch.Tensor, dout: torch.Tensor, du: torch.Tensor = None, dz: torch.Tensor = None,
+                 stage_events=None):
         """Gradients of the last forward_train on u: dout = dL/dh' bf16 [T, d] ->
-        du bf16 [T, d]; dw13, dw2, dcentroids (and dz [T, K] if given) filled."""
+        du bf16 [T, d]; dw13, dw2, dcentroids (and dz [T, K] if given) filled.
+        stage_events: optional 9 torch.cuda.Event(enable_timing=True) recorded
+        around the backward's eight stages on the current stream."""
         T = u.shape[0]
         du = torch.empty_like(u) if du is None else du
         ws = self.train_workspace(T)
-        grads = self._grads(dz)
+        grads = self._grads(dz, stage_events)
         _check(load_library().moe_layer_backward(ctypes.byref(self._desc), ctypes.byref(self._wt), _p(u), T,
                                                  _p(dout), _p(du), ctypes.byref(grads), _p(ws), ws.numel(),
                                                  _stream()), "moe_layer_backward")

@@ -466,7 +466,7 @@ class Backward:
 
 
 def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=1, topk_groups=1, fp8=True,
-                   route_all=None) -> Backward:
+                   route_all=None, stack=True) -> Backward:
     """Gradient of L = sum(G * h') for the layer h' (nlp-lineage page, "The
     notation") with the expert choice held fixed (readings in moe_oracle.c,
     [train]):
@@ -496,7 +496,9 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
     (FP64 throughout), the form the finite-difference pins check.
 
     expert_weights(e) -> (w1 [I,d], w3 [I,d], w2 [d,I]) as bf16 torch tensors or
-    fp32 arrays; e = N is the shared expert.
+    fp32 arrays; e = N is the shared expert; it is called only for experts
+    with rows. stack=False returns dw1, dw3, dw2 as dicts over the experts
+    with rows (for samples of a large layer) instead of stacked arrays.
     """
     import torch
     u_bits = as_bf16_bits(u_bf16)
@@ -523,10 +525,9 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
     Y_sh = None
     dX_rows = np.zeros((T * K, d))
     dX_sh = None
-    dW1, dW3, dW2 = [], [], []
+    dW1, dW3, dW2 = {}, {}, {}
+    I = _f32(expert_weights(N)[0]).shape[0]
     for e in range(N + 1):
-        w1, w3, w2 = (_f32(w) for w in expert_weights(e))
-        I = w1.shape[0]
         if e == N:
             rows = np.arange(T)
             toks = rows
@@ -537,11 +538,9 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
             gr = rgate[rows]
         out.rows[e] = toks
         n = toks.size
-        if n == 0:
-            dW1.append(np.zeros((I, d)))
-            dW3.append(np.zeros((I, d)))
-            dW2.append(np.zeros((d, I)))
+        if n == 0:   # an expert without rows: no product, zero weight gradients
             continue
+        w1, w3, w2 = (_f32(w) for w in expert_weights(e))
         X = uv[toks]
         if fp8:
             xq, xs = quant_1x128(u_bits[toks])
@@ -567,9 +566,9 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
             xq_t, xs_t = quant_128x1(X.astype(np.float32))
             hq1_t, hs1_t = quant_128x1(dHt1.astype(np.float32))
             hq3_t, hs3_t = quant_128x1(dHt3.astype(np.float32))
-            dW2.append(fp8_gemm_kscaled(yq_t, ys_t, aq_t, as_t))
-            dW1.append(fp8_gemm_kscaled(hq1_t, hs1_t, xq_t, xs_t))
-            dW3.append(fp8_gemm_kscaled(hq3_t, hs3_t, xq_t, xs_t))
+            dW2[e] = fp8_gemm_kscaled(yq_t, ys_t, aq_t, as_t)
+            dW1[e] = fp8_gemm_kscaled(hq1_t, hs1_t, xq_t, xs_t)
+            dW3[e] = fp8_gemm_kscaled(hq3_t, hs3_t, xq_t, xs_t)
             out.inter[e] = dict(Ht1=Ht1, Ht3=Ht3, Y=Y, dY=dY, dA=dA, dHt1=dHt1, dHt3=dHt3, dX=dX)
         else:
             W1, W3, W2 = (w.astype(np.float64) for w in (w1, w3, w2))
@@ -580,9 +579,9 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
             dA = dY @ W2
             dH1, dH3 = swiglu_backward(H1, H3, dA)
             dX = dH1 @ W1 + dH3 @ W3
-            dW2.append(dY.T @ A)
-            dW1.append(dH1.T @ X)
-            dW3.append(dH3.T @ X)
+            dW2[e] = dY.T @ A
+            dW1[e] = dH1.T @ X
+            dW3[e] = dH3.T @ X
             out.inter[e] = dict(Ht1=H1, Ht3=H3, Y=Y, dY=dY, dA=dA, dHt1=dH1, dHt3=dH3, dX=dX)
         if e == N:
             Y_sh, dX_sh = Y, dX
@@ -604,7 +603,12 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
         if tt.size:
             de[i] = (dz[tt, kk][:, None] * uv[tt]).sum(axis=0)
     out.du, out.dg, out.dz, out.de = du, dg, dz, de
-    out.dw1, out.dw3, out.dw2 = np.stack(dW1), np.stack(dW3), np.stack(dW2)
+    if stack:
+        def full(parts, shape):
+            return np.stack([parts[e] if e in parts else np.zeros(shape) for e in range(N + 1)])
+        out.dw1, out.dw3, out.dw2 = full(dW1, (I, d)), full(dW3, (I, d)), full(dW2, (d, I))
+    else:
+        out.dw1, out.dw3, out.dw2 = dW1, dW3, dW2
     return out
 
 

@@ -238,11 +238,11 @@ def test_training_entry_points_check_their_arguments(L):
         == M.MOE_ERR_WORKSPACE
     # the backward needs the transposed weights and every gradient buffer
     wt = M.LayerWeightsT(w13t=4096, w13t_scales=4096, w2t=4096, w2t_scales=4096)
-    g_missing = M.LayerGrads(dw13=4096, dw2=None, dcentroids=4096, dz=None)
+    g_missing = M.LayerGrads(dw13=4096, dw2=None, dcentroids=4096, dz=None, stage_events=None)
     assert L.moe_layer_backward(ctypes.byref(w), ctypes.byref(wt), p, T, p, p, ctypes.byref(g_missing), p, tr, s) \
         == M.MOE_ERR_INVALID_ARG
     wt0 = M.LayerWeightsT(w13t=None, w13t_scales=4096, w2t=4096, w2t_scales=4096)
-    g = M.LayerGrads(dw13=4096, dw2=4096, dcentroids=4096, dz=None)
+    g = M.LayerGrads(dw13=4096, dw2=4096, dcentroids=4096, dz=None, stage_events=None)
     assert L.moe_layer_backward(ctypes.byref(w), ctypes.byref(wt0), p, T, p, p, ctypes.byref(g), p, tr, s) \
         == M.MOE_ERR_INVALID_ARG
     # the training step needs fp32 centroids and masters
