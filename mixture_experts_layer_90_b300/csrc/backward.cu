@@ -15,9 +15,9 @@
 //
 // Kernels (rows r index the forward's permuted rows: routed rows grouped by
 // expert, then T rows of the shared expert):
-//   combine_bwd     one block per token: dg_{t,k} = G_t . y_{row(t,k)} and the
-//                   dgrad operand dY = g G_t per 1x128 tile (G_t's codes, g times
-//                   its scales)
+//   combine_bwd     one warp per (token, row): dg_{t,k} = G_t . y_{row(t,k)} and
+//                   the dgrad operand dY = g G_t per 1x128 tile (G_t's codes, g
+//                   times its scales)
 //   swiglu_bwd      one warp per (row, 128 outputs): dH from the stored bf16
 //                   H and dA, stored in bf16 and quantised per 1x128 tile
 //   kblock_offsets  each group's first 128-row block in the padded K layout
@@ -66,80 +66,53 @@ __device__ __forceinline__ float quant8_tile16(const float (&f)[8], uint2& codes
 
 constexpr int kMaxK = 16;
 
-// One block of 256 threads per token t. Thread i takes the 8-column chunks
-// i, i + 256, ... (a 1x128 tile is 16 consecutive threads).
+// One block of 32 (K + 1) threads per token t: warp k < K takes the routed row
+// of (t, k) -- dg_{t,k} = G_t . y_row and the row's dgrad operand -- and warp
+// K the shared expert's row. Lanes hold 8 consecutive columns; a 1x128 tile
+// is a half-warp, and a warp steps over d 256 columns at a time.
 // The dgrad operand of a routed row is the tile rule applied to g G_t: the
 // rule is scale-invariant (amax and every value scale by g), so its codes are
-// those of G_t's tile and its scale is g times G_t's. G_t's tiles are
-// quantised once and written to the shared expert's row (scale 1 x) and to
-// each of the token's K routed rows (scale g_k x).
-__global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __restrict__ G,
-                                                          const uint16_t* __restrict__ y,
-                                                          const float* __restrict__ gates,
-                                                          const int32_t* __restrict__ dest, int64_t T, int d, int K,
-                                                          int64_t R, uint8_t* __restrict__ qdy,
-                                                          float* __restrict__ sdy, float* __restrict__ row_gate,
-                                                          float* __restrict__ dg) {
-    __shared__ float red[8][kMaxK];
+// those of G_t's tile and its scale is g times G_t's. Every warp quantises
+// G_t's tiles itself (the same codes) and writes them to its row.
+__global__ void __launch_bounds__(32 * (kMaxK + 1)) combine_bwd_kernel(
+    const uint16_t* __restrict__ G, const uint16_t* __restrict__ y, const float* __restrict__ gates,
+    const int32_t* __restrict__ dest, int64_t T, int d, int K, int64_t R, uint8_t* __restrict__ qdy,
+    float* __restrict__ sdy, float* __restrict__ row_gate, float* __restrict__ dg) {
     const int64_t t = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    int64_t rows[kMaxK];
-    float g[kMaxK], acc[kMaxK];
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-        rows[k] = k < K ? int64_t(__ldg(dest + t * K + k)) : 0;
-        g[k] = k < K ? __ldg(gates + t * K + k) : 0.0f;
-        acc[k] = 0.0f;
-    }
-    const int64_t shared_row = T * K + t;
-    const int chunks = d / 8;
-    for (int c0 = 0; c0 < chunks; c0 += 256) {
-        const int c = c0 + tid;
-        const bool on = c < chunks;   // whole 16-lane tiles are on or off together (d % 128 == 0)
+    const int lane = threadIdx.x & 31, k = threadIdx.x >> 5;
+    const bool routed = k < K;
+    const int64_t row = routed ? int64_t(__ldg(dest + t * K + k)) : T * K + t;
+    const float g = routed ? __ldg(gates + t * K + k) : 1.0f;
+    const uint4* Gp = reinterpret_cast<const uint4*>(G + t * d);
+    const uint4* yp = reinterpret_cast<const uint4*>(y + row * d);
+    float acc = 0.0f;
+    for (int c = lane; c < d / 8; c += 32) {
         float gv[8];
-        {
-            const uint4 v = on ? __ldg(reinterpret_cast<const uint4*>(G + t * d) + c) : make_uint4(0, 0, 0, 0);
-            unpack8(v, gv);
-        }
-        const int64_t col = int64_t(c) * 8;
-        const int64_t kb = col / 128;
-        uint2 codes;
-        const float sc = quant8_tile16(gv, codes);
-        if (on) {
-            *reinterpret_cast<uint2*>(qdy + shared_row * d + col) = codes;
-            if ((lane & 15) == 0) sdy[kb * R + shared_row] = sc;
-        }
-#pragma unroll
-        for (int k = 0; k < kMaxK; ++k) {
-            if (k >= K) break;
+        unpack8(__ldg(Gp + c), gv);
+        if (routed) {
             float yv[8];
-            const uint4 v = on ? __ldg(reinterpret_cast<const uint4*>(y + rows[k] * d) + c) : make_uint4(0, 0, 0, 0);
-            unpack8(v, yv);
+            unpack8(__ldg(yp + c), yv);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[k] = fmaf(gv[i], yv[i], acc[k]);
-            if (on) {
-                *reinterpret_cast<uint2*>(qdy + rows[k] * d + col) = codes;
-                if ((lane & 15) == 0) sdy[kb * R + rows[k]] = __fmul_rn(g[k], sc);
-            }
+            for (int i = 0; i < 8; ++i) acc = fmaf(gv[i], yv[i], acc);
         }
+        uint2 codes;
+        // d % 256 == 0 (the layer's rule): every lane of the warp runs each step, as
+        // the shuffles of the tile's amax require
+        const float sc = quant8_tile16(gv, codes);
+        *reinterpret_cast<uint2*>(qdy + row * d + int64_t(c) * 8) = codes;
+        if ((lane & 15) == 0) sdy[(int64_t(c) / 16) * R + row] = routed ? __fmul_rn(g, sc) : sc;
     }
-    // dg: each thread's partial, a fixed xor tree inside the warp, warps in order
+    if (routed) {
+        // a fixed xor tree over the warp's partial sums
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-        if (k >= K) break;
-        float v = acc[k];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[w][k] = v;
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            dg[t * K + k] = acc;
+            row_gate[row] = g;
+        }
+    } else if (lane == 0) {
+        row_gate[row] = 1.0f;
     }
-    __syncthreads();
-    if (tid < K) {
-        float v = 0.0f;
-        for (int i = 0; i < 8; ++i) v += red[i][tid];
-        dg[t * K + tid] = v;
-        row_gate[__ldg(dest + t * K + tid)] = __ldg(gates + t * K + tid);
-    }
-    if (tid == 0) row_gate[shared_row] = 1.0f;
 }
 
 // One warp per (row r, pair p of 128-column blocks): lanes hold 4 of the 128
@@ -513,7 +486,8 @@ cudaError_t launch_combine_bwd(const uint16_t* G, const uint16_t* y, const float
                                int64_t T, int d, int K, int64_t R, uint8_t* qdy, float* sdy, float* row_gate,
                                float* dg, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    combine_bwd_kernel<<<unsigned(T), 256, 0, stream>>>(G, y, gates, dest, T, d, K, R, qdy, sdy, row_gate, dg);
+    combine_bwd_kernel<<<unsigned(T), 32 * (K + 1), 0, stream>>>(G, y, gates, dest, T, d, K, R, qdy, sdy, row_gate,
+                                                                 dg);
     return cudaGetLastError();
 }
 
