@@ -38,7 +38,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;   // shared-memory ring depth (the weight gradient's: 2)
 constexpr int kBM = 128, kBN = 256;
 constexpr int kABytes = kBM * 128, kBBytes = kBN * 128;
 constexpr int kEpiWarps = 16, kThreads = (kEpiWarps + 3) * 32;
@@ -67,12 +67,26 @@ struct Smem {
     int prefix[kMaxGroups + 1];
     int offs[kMaxGroups + 1];   // row offsets of the groups (weight gradient: K-block offsets)
 };
-constexpr size_t kRingBytes = size_t(kStages) * (kABytes + kBBytes);
+// The weight gradient's tiles have 2-3 K blocks and 128 KB of fp32 output each:
+// a 2-stage ring, and 4 KB per epilogue warp to stage its output for TMA stores.
 template <int kMode>
-constexpr size_t smem_bytes() {
-    return kRingBytes + sizeof(Smem<kMode>) + 1024;
+__host__ __device__ constexpr int stages_of() {
+    return kMode == kModeFP8W ? 2 : kStages;
 }
-static_assert(smem_bytes<kModeFP8W>() <= 227 * 1024, "shared memory");
+template <int kMode>
+__host__ __device__ constexpr size_t ring_bytes() {
+    return size_t(stages_of<kMode>()) * (kABytes + kBBytes);
+}
+constexpr size_t kStageBytes = 4096;   // one warp's 32 rows x 128 bytes, 128-byte swizzle
+template <int kMode>
+__host__ __device__ constexpr size_t staging_offset() {   // from the ring's start, 1024-byte aligned
+    return (ring_bytes<kMode>() + sizeof(Smem<kMode>) + 1023) / 1024 * 1024;
+}
+template <int kMode>
+__host__ __device__ constexpr size_t smem_bytes() {
+    return staging_offset<kMode>() + (kMode == kModeFP8W ? kEpiWarps * kStageBytes : 0) + 1024;
+}
+static_assert(smem_bytes<kModeFP8W>() <= 227 * 1024 && smem_bytes<kModeFP8>() <= 227 * 1024, "shared memory");
 static_assert(offsetof(Smem<kModeFP8W>, scales) % 16 == 0 && sizeof(ScaleSlot<kBN>) % 16 == 0, "scale slots");
 
 struct Item {
@@ -93,7 +107,15 @@ __device__ __forceinline__ Item decode(int item, const S& s, int G, int n_tiles_
     int local = item - s.prefix[lo];
     it.sp = local % splits;
     local /= splits;
-    int m_tiles = m_tiles_fixed > 0 ? m_tiles_fixed : (s.offs[lo + 1] - s.offs[lo] + kBM - 1) / kBM;
+    if (m_tiles_fixed > 0) {
+        // weight gradient: N tiles first, so that the CTAs running side by side write
+        // whole rows of the fp32 output (its HBM stream) rather than scattered pieces
+        it.nt = local % n_tiles_n;
+        it.mt = local / n_tiles_n;
+        return it;
+    }
+    // row tiles first: the CTAs running side by side share the weight tiles (L2)
+    int m_tiles = (s.offs[lo + 1] - s.offs[lo] + kBM - 1) / kBM;
     it.mt = local % m_tiles;
     it.nt = local / m_tiles;
     return it;
@@ -113,14 +135,16 @@ __device__ __forceinline__ void st_global_32B(void* p, const uint32_t* w) {   //
 template <int kMode, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem<kMode>& s = *reinterpret_cast<Smem<kMode>*>(ring + kRingBytes);
+    Smem<kMode>& s = *reinterpret_cast<Smem<kMode>*>(ring + ring_bytes<kMode>());
     constexpr bool kW = kMode == kModeFP8W;         // weight gradient: groups split K
     constexpr bool kScaled = kMode != kModeBF16;     // FP8 operands with scales
+    constexpr int kSt = stages_of<kMode>();
+    const uint32_t staging = smem_u32(ring + staging_offset<kMode>());
     const uint32_t ringA = smem_u32(ring);
-    const uint32_t ringB = ringA + kStages * kABytes;
+    const uint32_t ringB = ringA + kSt * kABytes;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = args.G;
@@ -132,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------- prologue ----------------
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kSt; ++i) {
             mbar_init(smem_u32(&s.full[i]), 1);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
@@ -210,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int armed[kStages] = {0, 0, 0, 0};
+            int armed[kStages] = {0, 0, 0, 0};   // the first kSt are used
             bool stop = false;
             for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
                 const Item it = decode(item, s, G, n_tiles_n, splits, m_fixed);
@@ -236,14 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rep = 0;
                         ++ka;
                     }
-                    if (++stage == kStages) {
+                    if (++stage == kSt) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
             // never leave the block while a copy into its shared memory is in flight
-            for (int i = 0; i < kStages; ++i)
+            for (int i = 0; i < kSt; ++i)
                 if (armed[i] > 0) mbar_wait_limit(smem_u32(&s.full[i]), uint32_t(armed[i] - 1) & 1u, 200000000ull);
         }
         __syncwarp();
@@ -368,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_commit(smem_u32(&s.tfull[buf]));
                         acc_iter += 1;
                     }
-                    if (++stage == kStages) {
+                    if (++stage == kSt) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -421,22 +445,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float2 sa2 = make_float2(sa_v, sa_v);
                     tc_fence_after();
                     const uint32_t col = lane_addr + buf * kBN + slice;
+                    // 4 columns per TMEM load: the per-column scales leave no registers for
+                    // wider loads (16 columns spilled, and ran 1.6x slower)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[16];
-                        tmem_ld_16(col + c * 16, r);
+                    for (int c = 0; c < 16; ++c) {
+                        uint32_t r[4];
+                        tmem_ld_4(col + c * 4, r);
                         tmem_wait_ld(r);
-                        if (c == 3) {
+                        if (c == 15) {
                             tc_fence_before();
                             mbar_arrive(smem_u32(&s.tempty[buf]));
                         }
-                        const float2* sbp = reinterpret_cast<const float2*>(&s.scales[sslot].sb[slice + 16 * c]);
+                        const float2* sbp = reinterpret_cast<const float2*>(&s.scales[sslot].sb[slice + 4 * c]);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
+                        for (int i = 0; i < 2; ++i) {
                             const float2 f2 = __fmul2_rn(sbp[i], sa2);
-                            acc2[c * 8 + i] = __ffma2_rn(
+                            acc2[c * 2 + i] = __ffma2_rn(
                                 make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), f2,
-                                acc2[c * 8 + i]);
+                                acc2[c * 2 + i]);
                         }
                     }
                     // the slot is released after the last column scale was read
@@ -647,38 +673,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       w + 8 * i);
                 }
             } else if (kW) {
-                // weight gradient, fp32 [G][M][Nd]: per 32-column half, four lanes swap
-                // 32-byte pieces (a 4x4 transpose by two xor-shuffle rounds), so that in
-                // store i the lanes 4a..4a+3 write the 128 bytes of row 4a+i: every store
-                // instruction of the warp writes 8 whole 128-byte lines
-                const bool b0 = lane & 1, b1 = lane & 2;
-                const int64_t rbase = int64_t(it.g) * args.M_total + it.mt * kBM + q * 32 + (lane & ~3);
-                float* cbase = reinterpret_cast<float*>(args.C) + int64_t(it.nt) * kBN + slice + 8 * (lane & 3);
+                // weight gradient, fp32 [G][M][Nd], by TMA stores: the warp's 32 rows x 32
+                // columns at a time go to its 4 KB staging buffer (lane = row, 16-byte
+                // chunk c at c ^ (row % 8): the 128-byte swizzle of the store's tensor map,
+                // no bank conflicts), and lane 0 stores the box while the warp goes on
+                const uint32_t buf = staging + uint32_t(warp) * uint32_t(kStageBytes);
+                const int32_t y0 = int32_t(int64_t(it.g) * args.M_total + it.mt * kBM + q * 32);
+                const int32_t x0 = int32_t(it.nt * kBN + slice);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    float* x = acc + 32 * half;   // swapped in place
+                    if (lane == 0) bulk_wait_read_all();   // the buffer's last store has read it
+                    __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 4; c += 2)
-#pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            const float v = __shfl_xor_sync(0xffffffffu, b0 ? x[8 * c + r] : x[8 * c + 8 + r], 1);
-                            if (b0) x[8 * c + r] = v;
-                            else x[8 * c + 8 + r] = v;
-                        }
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            const float v = __shfl_xor_sync(0xffffffffu, b1 ? x[8 * c + r] : x[8 * c + 16 + r], 2);
-                            if (b1) x[8 * c + r] = v;
-                            else x[8 * c + 16 + r] = v;
-                        }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) w[j] = __float_as_uint(x[8 * i + j]);
-                        st_global_32B(cbase + (rbase + i) * args.Nd + 32 * half, w);
+                    for (int c = 0; c < 8; ++c) {
+                        const float* v = acc + 32 * half + 4 * c;
+                        const uint32_t dst = buf + uint32_t(lane) * 128u + uint32_t((c ^ (lane & 7)) * 16);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(v[0]), "f"(v[1]),
+                                     "f"(v[2]), "f"(v[3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, buf, x0 + 32 * half, y0);
+                        bulk_commit();
                     }
                 }
             } else if (valid) {
@@ -698,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- teardown ----------------
+    if (kW && warp < kEpiWarps && lane == 0) bulk_wait_all();   // every TMA store of this warp written
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -740,31 +759,48 @@ bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inne
 }
 
 template <int kMode, int kEpi>
-static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
-                          cudaStream_t stream) {
+static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
+                          int grid, cudaStream_t stream) {
     static PerDeviceOnce once;
     constexpr size_t kSmemBytes = smem_bytes<kMode>();
     cudaError_t e = allow_smem(once, grouped_gemm_kernel<kMode, kEpi>, int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<kMode, kEpi><<<grid, kThreads, kSmemBytes, stream>>>(a, b, args);
+    grouped_gemm_kernel<kMode, kEpi><<<grid, kThreads, kSmemBytes, stream>>>(a, b, c, args);
     return cudaGetLastError();
 }
 
 cudaError_t run_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, const CUtensorMap* c) {
+    const CUtensorMap& cm = c ? *c : a;   // only the weight gradient stores through a tensor map
     if (mode == kModeFP8W) {
-        if (args.epilogue == MOE_EPI_F32) return launch<kModeFP8W, MOE_EPI_F32>(a, b, args, grid, stream);
+        if (args.epilogue == MOE_EPI_F32 && c) return launch<kModeFP8W, MOE_EPI_F32>(a, b, cm, args, grid, stream);
         return cudaErrorInvalidValue;
     }
     if (mode == kModeFP8) {
-        if (args.epilogue == MOE_EPI_SWIGLU_FP8) return launch<kModeFP8, MOE_EPI_SWIGLU_FP8>(a, b, args, grid, stream);
-        if (args.epilogue == MOE_EPI_BF16) return launch<kModeFP8, MOE_EPI_BF16>(a, b, args, grid, stream);
+        if (args.epilogue == MOE_EPI_SWIGLU_FP8)
+            return launch<kModeFP8, MOE_EPI_SWIGLU_FP8>(a, b, cm, args, grid, stream);
+        if (args.epilogue == MOE_EPI_BF16) return launch<kModeFP8, MOE_EPI_BF16>(a, b, cm, args, grid, stream);
         return cudaErrorInvalidValue;
     }
-    if (args.epilogue == MOE_EPI_SWIGLU_BF16) return launch<kModeBF16, MOE_EPI_SWIGLU_BF16>(a, b, args, grid, stream);
-    if (args.epilogue == MOE_EPI_BF16) return launch<kModeBF16, MOE_EPI_BF16>(a, b, args, grid, stream);
-    if (args.epilogue == MOE_EPI_F32) return launch<kModeBF16, MOE_EPI_F32>(a, b, args, grid, stream);
+    if (args.epilogue == MOE_EPI_SWIGLU_BF16) return launch<kModeBF16, MOE_EPI_SWIGLU_BF16>(a, b, cm, args, grid, stream);
+    if (args.epilogue == MOE_EPI_BF16) return launch<kModeBF16, MOE_EPI_BF16>(a, b, cm, args, grid, stream);
+    if (args.epilogue == MOE_EPI_F32) return launch<kModeBF16, MOE_EPI_F32>(a, b, cm, args, grid, stream);
     return cudaErrorInvalidValue;
+}
+
+// 2-D fp32 row-major store map: `rows` rows of `cols` floats, box 32 x 32,
+// 128-byte swizzle (the weight gradient's staged output).
+bool make_f32_store_map(CUtensorMap* tm, void* base, uint64_t cols, uint64_t rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 int gemm_max_groups() { return kMaxGroups; }

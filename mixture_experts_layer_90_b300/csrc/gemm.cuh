@@ -40,8 +40,10 @@ struct GemmArgs {
 bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inner, uint64_t rows,
                      uint64_t row_bytes, uint32_t box_rows);
 
+// c: the output's store map (kModeFP8W only, make_f32_store_map); nullptr otherwise.
 cudaError_t run_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
-                             cudaStream_t stream);
+                             cudaStream_t stream, const CUtensorMap* c = nullptr);
+bool make_f32_store_map(CUtensorMap* tm, void* base, uint64_t cols, uint64_t rows);
 
 int gemm_max_groups();
 

@@ -69,9 +69,10 @@ moe_status check_ws(void* ws, size_t bytes, size_t need, const char* who) {
 
 moe_status wgrad_gemm(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb, const int32_t* kofs,
                       int G, int M, int Nd, int64_t Kp, float* C, moe_stream_t stream) {
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     if (!moe::make_kmajor_map(&ta, A, false, uint64_t(Kp), uint64_t(M), uint64_t(Kp), 128) ||
-        !moe::make_kmajor_map(&tb, B, false, uint64_t(Kp), uint64_t(Nd), uint64_t(Kp), 256))
+        !moe::make_kmajor_map(&tb, B, false, uint64_t(Kp), uint64_t(Nd), uint64_t(Kp), 256) ||
+        !moe::make_f32_store_map(&tc, C, uint64_t(Nd), uint64_t(G) * M))
         return fail(MOE_ERR_CUDA, "fp8_grouped_gemm_wgrad: tensor map encoding failed");
     moe::GemmArgs a{};
     a.group_offsets = kofs;
@@ -88,7 +89,7 @@ moe_status wgrad_gemm(const uint8_t* A, const float* sa, const uint8_t* B, const
     a.lda_s = M;
     a.sb = sb;
     a.C = C;
-    CUDA_OK(moe::run_grouped_gemm(moe::kModeFP8W, ta, tb, a, moe::num_sms(), stream));
+    CUDA_OK(moe::run_grouped_gemm(moe::kModeFP8W, ta, tb, a, moe::num_sms(), stream, &tc));
     return MOE_OK;
 }
 
