@@ -359,7 +359,9 @@ moe_status moe_layer_forward_host_pipelined(const moe_layer_weights* w, const ui
  *             dW2 = dY^T A and dW13 = dH^T X contract over the expert's own
  *             tokens: both operands quantised per (128 tokens, column), A
  *             recomputed in fp32 from H, X = u of the rows; fp32 out;
- *   gates     S = sum_k s_k, c = sum_k g_k dg_k, dz_k = (dg_k - c) / S s_k (1 - s_k);
+ *   gates     S = sum_k s_k, c = sum_k g_k dg_k, dz_k = (dg_k - c) / S s'(z_k), with the
+ *             sigmoid's derivative s (1 - s) evaluated from the logit as
+ *             e^-|z| / (1 + e^-|z|)^2 (no cancellation in 1 - s when s is near 1);
  *   tokens    du_t = G_t + dX_shared,t + sum_k dX_row(t,k) + sum_k dz_k e_idx(t,k)  (bf16);
  *   centroids de_i = sum over the (t, k) routed to i of dz_{t,k} u_t  (fp32);
  *   bias      no gradient: it moves by the load rule after the step.
@@ -403,7 +405,8 @@ typedef struct {
 size_t moe_layer_train_workspace_size(const moe_layer_weights* w, int64_t T);
 
 /* moe_layer_forward that also keeps, in the workspace, what the backward
- * reads: the affinities s [T, N] and GEMM 1's products H [T*K+T, 2I] in bf16. */
+ * reads: the affinities s and gate logits z [T, N] and GEMM 1's products
+ * H [T*K+T, 2I] in bf16. */
 moe_status moe_layer_forward_train(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
                                    const moe_layer_outputs* outs, int update_bias, void* workspace,
                                    size_t workspace_bytes, moe_stream_t stream);
@@ -448,7 +451,8 @@ enum {
     MOE_TRAIN_DY_S = 12,       /* fp32 [d/128, R] its 1x128 scales */
     MOE_TRAIN_DH_Q = 13,       /* e4m3 [R, 2I] the operand dH of dX = dH W13 */
     MOE_TRAIN_DH_S = 14,       /* fp32 [2I/128, R] its 1x128 scales */
-    MOE_TRAIN_ROW_GATE = 15    /* fp32 [R] the gate of each row (1 for the shared expert's) */
+    MOE_TRAIN_ROW_GATE = 15,   /* fp32 [R] the gate of each row (1 for the shared expert's) */
+    MOE_TRAIN_LOGITS = 16      /* fp32 [T, N] the gate logits z (s = sigmoid(z)) */
 };
 moe_status moe_layer_train_buffer(const moe_layer_weights* w, int64_t T, int which, size_t* offset,
                                   size_t* bytes);

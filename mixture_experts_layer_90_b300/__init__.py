@@ -76,7 +76,7 @@ class LayerMasters(ctypes.Structure):
 
 
 TRAIN_BUFFERS = {"H": 0, "scores": 1, "dg": 2, "dA": 3, "dH": 4, "dX": 5, "offsets": 6, "perm_token": 7,
-                 "dest_row": 8, "y": 9, "kofs": 10, "dy_q": 11, "dy_s": 12, "dh_q": 13, "dh_s": 14, "row_gate": 15}
+                 "dest_row": 8, "y": 9, "kofs": 10, "dy_q": 11, "dy_s": 12, "dh_q": 13, "dh_s": 14, "row_gate": 15, "logits": 16}
 
 
 class LayerOutputs(ctypes.Structure):

@@ -154,10 +154,11 @@ moe_status moe_route_prepare_centroids(const void* centroids, int centroid_dtype
     return MOE_OK;
 }
 
-moe_status moe_route_prepared(const uint16_t* u, int64_t T, int d, const void* prepared, int centroid_dtype,
-                              const float* bias, int N, int K, int n_groups, int topk_groups, int32_t* topk_idx,
-                              float* gates, int32_t* loads, float* scores, void* workspace, size_t workspace_bytes,
-                              moe_stream_t stream) {
+// logits (optional, the training forward's): the fp32 gate logits [T, N]
+static moe_status route_prepared_impl(const uint16_t* u, int64_t T, int d, const void* prepared, int centroid_dtype,
+                                      const float* bias, int N, int K, int n_groups, int topk_groups,
+                                      int32_t* topk_idx, float* gates, int32_t* loads, float* scores,
+                                      void* workspace, size_t workspace_bytes, moe_stream_t stream, float* logits) {
     STATUS_OK(check_route(u, T, d, prepared, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates,
                           loads));
     const moe::RoutePlan plan = moe::plan_route(T, d, N, centroid_dtype);
@@ -167,13 +168,23 @@ moe_status moe_route_prepared(const uint16_t* u, int64_t T, int d, const void* p
         return fail(MOE_ERR_WORKSPACE, "moe_route_prepared: workspace needs %zu bytes, 256-byte aligned",
                     plan.zpart_bytes);
     CUDA_OK(moe::launch_route(u, T, d, prepared, bias, N, K, n_groups > 1 ? n_groups : 1,
-                              n_groups > 1 ? topk_groups : 1, topk_idx, gates, loads, scores, workspace, plan, stream));
+                              n_groups > 1 ? topk_groups : 1, topk_idx, gates, loads, scores, workspace, plan, stream,
+                              logits));
     return MOE_OK;
 }
 
-moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype, const float* bias,
-                     int N, int K, int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
-                     float* scores, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+moe_status moe_route_prepared(const uint16_t* u, int64_t T, int d, const void* prepared, int centroid_dtype,
+                              const float* bias, int N, int K, int n_groups, int topk_groups, int32_t* topk_idx,
+                              float* gates, int32_t* loads, float* scores, void* workspace, size_t workspace_bytes,
+                              moe_stream_t stream) {
+    return route_prepared_impl(u, T, d, prepared, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates,
+                               loads, scores, workspace, workspace_bytes, stream, nullptr);
+}
+
+static moe_status route_impl(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype,
+                             const float* bias, int N, int K, int n_groups, int topk_groups, int32_t* topk_idx,
+                             float* gates, int32_t* loads, float* scores, void* workspace, size_t workspace_bytes,
+                             moe_stream_t stream, float* logits) {
     STATUS_OK(check_route(u, T, d, centroids, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates,
                           loads));
     const moe::RoutePlan plan = moe::plan_route(T, d, N, centroid_dtype);
@@ -182,8 +193,15 @@ moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids,
     uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
     if (T > 0) CUDA_OK(moe::launch_route_prepare(centroids, centroid_dtype, N, d, plan, ws, stream));
     CUDA_OK(moe::launch_route(u, T, d, ws, bias, N, K, n_groups > 1 ? n_groups : 1, n_groups > 1 ? topk_groups : 1,
-                              topk_idx, gates, loads, scores, ws + plan.split_bytes, plan, stream));
+                              topk_idx, gates, loads, scores, ws + plan.split_bytes, plan, stream, logits));
     return MOE_OK;
+}
+
+moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype, const float* bias,
+                     int N, int K, int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
+                     float* scores, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return route_impl(u, T, d, centroids, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads,
+                      scores, workspace, workspace_bytes, stream, nullptr);
 }
 
 size_t moe_route_balance_stats_workspace_size(int64_t T, int N, int64_t seq_len) {
@@ -403,11 +421,12 @@ size_t moe_layer_host_workspace_size(const moe_layer_weights* w, int64_t T) {
     return w ? layer_ws(w, T, 1).total : 0;
 }
 
-// scores / h_out (training forward, FP8 only): the affinities [T, N] and GEMM 1's
-// products in bf16 [R, 2I] are kept there.
+// scores / logits / h_out (training forward, FP8 only): the affinities and the gate
+// logits [T, N] and GEMM 1's products in bf16 [R, 2I] are kept there.
 static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
                                 const moe_layer_outputs* outs, int update_bias, uint8_t* ws, const LayerWs& L,
-                                moe_stream_t stream, float* scores = nullptr, uint16_t* h_out = nullptr) {
+                                moe_stream_t stream, float* scores = nullptr, uint16_t* h_out = nullptr,
+                                float* logits = nullptr) {
     const int K = w->K, N = w->N, d = w->d, I = w->I;
     const int64_t R = T * K + T;
     if (T == 0) {
@@ -430,12 +449,12 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
     };
     STATUS_OK(mark(0));
     if (w->centroids_prepared)
-        STATUS_OK(moe_route_prepared(u, T, d, w->centroids_prepared, w->centroid_dtype, w->bias, N, K, w->n_groups,
-                                     w->topk_groups, topk, gates, loads, scores, ws + L.route, L.perm - L.route,
-                                     stream));
+        STATUS_OK(route_prepared_impl(u, T, d, w->centroids_prepared, w->centroid_dtype, w->bias, N, K, w->n_groups,
+                                      w->topk_groups, topk, gates, loads, scores, ws + L.route, L.perm - L.route,
+                                      stream, logits));
     else
-        STATUS_OK(moe_route(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups,
-                            topk, gates, loads, scores, ws + L.route, L.perm - L.route, stream));
+        STATUS_OK(route_impl(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups,
+                             topk, gates, loads, scores, ws + L.route, L.perm - L.route, stream, logits));
     STATUS_OK(mark(1));
     STATUS_OK(moe_permute(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
                           reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,

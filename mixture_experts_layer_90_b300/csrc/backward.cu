@@ -293,7 +293,8 @@ __global__ void __launch_bounds__(256) quant_t_kernel(const QuantTArgs a) {
 __global__ void __launch_bounds__(256) unpermute_bwd_kernel(
     const uint16_t* __restrict__ G, const uint16_t* __restrict__ dX, const int32_t* __restrict__ dest,
     const int32_t* __restrict__ topk, const float* __restrict__ gates, const float* __restrict__ scores,
-    const float* __restrict__ dg, const void* __restrict__ centroids, int centroid_f32, int64_t T, int d, int N,
+    const float* __restrict__ logits, const float* __restrict__ dg, const void* __restrict__ centroids,
+    int centroid_f32, int64_t T, int d, int N,
     int K, uint16_t* __restrict__ du, float* __restrict__ dz_row, float* __restrict__ dz_out) {
     __shared__ float dz[kMaxK];
     __shared__ int64_t rows[kMaxK];
@@ -301,17 +302,19 @@ __global__ void __launch_bounds__(256) unpermute_bwd_kernel(
     const int64_t t = blockIdx.x;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        float S = 0.0f, c = 0.0f, s[kMaxK];
+        float S = 0.0f, c = 0.0f;
         for (int k = 0; k < K; ++k) {
             const int e = topk[t * K + k];
             ids[k] = e;
             rows[k] = dest[t * K + k];
-            s[k] = scores[t * N + e];
-            S += s[k];
+            S += scores[t * N + e];
             c = fmaf(gates[t * K + k], dg[t * K + k], c);
         }
         for (int k = 0; k < K; ++k) {
-            const float v = __fdiv_rn(dg[t * K + k] - c, S) * s[k] * (1.0f - s[k]);
+            // s'(z) = s (1 - s) from the logit: e^-|z| / (1 + e^-|z|)^2, accurate where s is near 1
+            const float ez = expf(-fabsf(logits[t * N + ids[k]]));
+            const float dsig = __fdiv_rn(ez, (1.0f + ez) * (1.0f + ez));
+            const float v = __fdiv_rn(dg[t * K + k] - c, S) * dsig;
             dz[k] = v;
             dz_row[rows[k]] = v;
             if (dz_out) dz_out[t * K + k] = v;
@@ -521,11 +524,11 @@ cudaError_t launch_quant_t(int src_kind, const int32_t* offsets, const int32_t* 
 }
 
 cudaError_t launch_unpermute_bwd(const uint16_t* G, const uint16_t* dX, const int32_t* dest, const int32_t* topk,
-                                 const float* gates, const float* scores, const float* dg, const void* centroids,
-                                 int centroid_f32, int64_t T, int d, int N, int K, uint16_t* du, float* dz_row,
-                                 float* dz_out, cudaStream_t stream) {
+                                 const float* gates, const float* scores, const float* logits, const float* dg,
+                                 const void* centroids, int centroid_f32, int64_t T, int d, int N, int K, uint16_t* du,
+                                 float* dz_row, float* dz_out, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    unpermute_bwd_kernel<<<unsigned(T), 256, 0, stream>>>(G, dX, dest, topk, gates, scores, dg, centroids,
+    unpermute_bwd_kernel<<<unsigned(T), 256, 0, stream>>>(G, dX, dest, topk, gates, scores, logits, dg, centroids,
                                                           centroid_f32, T, d, N, K, du, dz_row, dz_out);
     return cudaGetLastError();
 }

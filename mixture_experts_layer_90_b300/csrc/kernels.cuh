@@ -26,9 +26,11 @@ size_t prepared_centroid_bytes(int d, int N, int centroid_dtype);
 RoutePlan plan_route(int64_t T, int d, int N, int centroid_dtype);
 cudaError_t launch_route_prepare(const void* centroids, int centroid_dtype, int N, int d, const RoutePlan& plan,
                                  void* prepared, cudaStream_t stream);
+// logits (optional): the fp32 gate logits z [T, N] (the training forward keeps them)
 cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* prepared, const float* bias, int N, int K,
                          int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
-                         float* scores, void* zpart_ws, const RoutePlan& plan, cudaStream_t stream);
+                         float* scores, void* zpart_ws, const RoutePlan& plan, cudaStream_t stream,
+                         float* logits = nullptr);
 
 // Permutation (stable counting sort by expert) and row scatter.
 size_t permute_ws_bytes(int64_t T, int N);
@@ -58,7 +60,8 @@ cudaError_t launch_quant_t(int src_kind, const int32_t* offsets, const int32_t* 
                            const int32_t* perm_token, const float* row_gate, const uint16_t* src, int C,
                            int64_t Kp, uint8_t* q, float* s, cudaStream_t stream);
 cudaError_t launch_unpermute_bwd(const uint16_t* G, const uint16_t* dX, const int32_t* dest, const int32_t* topk,
-                                 const float* gates, const float* scores, const float* dg, const void* centroids,
+                                 const float* gates, const float* scores, const float* logits, const float* dg,
+                                 const void* centroids,
                                  int centroid_f32, int64_t T, int d, int N, int K, uint16_t* du, float* dz_row,
                                  float* dz_out, cudaStream_t stream);
 cudaError_t launch_centroid_grad(const uint16_t* u, const int32_t* offsets, const int32_t* perm_token,

@@ -73,7 +73,8 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
                                                            int n_pad, const float* __restrict__ bias, int N, int K,
                                                            int n_groups, int topk_groups, int32_t* __restrict__ topk_idx,
                                                            float* __restrict__ gates, int32_t* __restrict__ loads,
-                                                           float* __restrict__ scores) {
+                                                           float* __restrict__ scores,
+                                                           float* __restrict__ logits) {
     extern __shared__ int sm[];
     int* hist = sm;                                            // [N]
     float* keys_sm = reinterpret_cast<float*>(sm + N);         // [8][N] when grouped
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
             // chosen, last, so every token keeps exactly K valid experts
             key[j] = (i < N && kv == kv) ? kv : -INFINITY;
             if (scores && i < N) scores[t * N + i] = s[j];
+            if (logits && i < N) logits[t * N + i] = z;
         }
         if (n_groups > 1) {
             float* ks = keys_sm + w * N;
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
 template <int J>
 cudaError_t launch_select(const float* zpart, int splits, int64_t T, int n_pad, const float* bias, int N, int K,
                           int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
-                          float* scores, cudaStream_t stream) {
+                          float* scores, float* logits, cudaStream_t stream) {
     const size_t smem = size_t(N) * 4 + (n_groups > 1 ? size_t(8) * N * 4 : 0);
     static PerDeviceOnce once;
     cudaError_t e = allow_smem(once, route_select_kernel<J>, 48 * 1024);
@@ -224,7 +226,8 @@ cudaError_t launch_select(const float* zpart, int splits, int64_t T, int n_pad, 
     const int64_t cap = int64_t(num_sms()) * 8;
     if (blocks > cap) blocks = cap;
     route_select_kernel<J><<<int(blocks), 256, smem, stream>>>(zpart, splits, T, n_pad, bias, N, K, n_groups,
-                                                                topk_groups, topk_idx, gates, loads, scores);
+                                                                topk_groups, topk_idx, gates, loads, scores,
+                                                                logits);
     return cudaGetLastError();
 }
 
@@ -281,7 +284,7 @@ cudaError_t launch_route_prepare(const void* centroids, int centroid_dtype, int 
 
 cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* prepared, const float* bias, int N, int K,
                          int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
-                         float* scores, void* zpart_ws, const RoutePlan& plan, cudaStream_t stream) {
+                         float* scores, void* zpart_ws, const RoutePlan& plan, cudaStream_t stream, float* logits) {
     cudaError_t e = cudaMemsetAsync(loads, 0, sizeof(int32_t) * N, stream);
     if (e != cudaSuccess || T == 0) return e;
     const uint16_t* esplit = reinterpret_cast<const uint16_t*>(prepared);
@@ -309,12 +312,12 @@ cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* prepar
     if ((e = run_grouped_gemm(kModeBF16, ta, tb, a, grid, stream)) != cudaSuccess) return e;
 
     const int Jneed = (N + 31) / 32;
-    if (Jneed <= 1) return launch_select<1>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, stream);
-    if (Jneed <= 2) return launch_select<2>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, stream);
-    if (Jneed <= 4) return launch_select<4>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, stream);
-    if (Jneed <= 8) return launch_select<8>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, stream);
-    if (Jneed <= 16) return launch_select<16>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, stream);
-    return launch_select<32>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, stream);
+    if (Jneed <= 1) return launch_select<1>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, logits, stream);
+    if (Jneed <= 2) return launch_select<2>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, logits, stream);
+    if (Jneed <= 4) return launch_select<4>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, logits, stream);
+    if (Jneed <= 8) return launch_select<8>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, logits, stream);
+    if (Jneed <= 16) return launch_select<16>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, logits, stream);
+    return launch_select<32>(zpart, plan.splits, T, plan.n_pad, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads, scores, logits, stream);
 }
 
 }  // namespace moe

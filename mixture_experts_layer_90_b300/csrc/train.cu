@@ -8,7 +8,7 @@ namespace {
 // The training workspace: the forward's (LayerWs), then the buffers below.
 struct TrainWs {
     LayerWs fwd;
-    size_t H, scores, row_gate, dg, qdy, sdy, dA, dH, qdh, sdh, dX, kofs, dz_row;
+    size_t H, scores, logits, row_gate, dg, qdy, sdy, dA, dH, qdh, sdh, dX, kofs, dz_row;
     size_t qyt, syt, qat, sat, qht, sht, qxt, sxt;
     int64_t Kp;   // padded token rows of the weight-gradient operands
     size_t total;
@@ -30,6 +30,7 @@ TrainWs train_ws(const moe_layer_weights* w, int64_t T) {
     };
     W.H = take(size_t(R) * 2 * I * 2);
     W.scores = take(size_t(T) * w->N * 4);
+    W.logits = take(size_t(T) * w->N * 4);
     W.row_gate = take(size_t(R) * 4);
     W.dg = take(size_t(T) * w->K * 4);
     W.qdy = take(size_t(R) * d);
@@ -117,6 +118,7 @@ moe_status layer_backward(const moe_layer_weights* w, const moe_layer_weights_t*
     const uint16_t* y = reinterpret_cast<const uint16_t*>(ws + L.y);
     const uint16_t* H = reinterpret_cast<const uint16_t*>(ws + W.H);
     const float* scores = reinterpret_cast<const float*>(ws + W.scores);
+    const float* logits = reinterpret_cast<const float*>(ws + W.logits);
     float* row_gate = reinterpret_cast<float*>(ws + W.row_gate);
     float* dg = reinterpret_cast<float*>(ws + W.dg);
     uint8_t* qdy = ws + W.qdy;
@@ -149,7 +151,7 @@ moe_status layer_backward(const moe_layer_weights* w, const moe_layer_weights_t*
                             nullptr, nullptr, stream));
     STATUS_OK(mark(4));
     // gates and du
-    CUDA_OK(moe::launch_unpermute_bwd(dout, dX, dest, topk, gates, scores, dg, w->centroids,
+    CUDA_OK(moe::launch_unpermute_bwd(dout, dX, dest, topk, gates, scores, logits, dg, w->centroids,
                                       w->centroid_dtype == MOE_DTYPE_F32, T, d, N, K, du, dz_row, gr->dz, stream));
     CUDA_OK(moe::launch_centroid_grad(u, offsets, perm_token, dz_row, N, d, gr->dcentroids, stream));
     STATUS_OK(mark(5));
@@ -226,6 +228,7 @@ moe_status moe_layer_train_buffer(const moe_layer_weights* w, int64_t T, int whi
         case MOE_TRAIN_DH_Q: *offset = W.qdh; *bytes = size_t(R) * 2 * I; break;
         case MOE_TRAIN_DH_S: *offset = W.sdh; *bytes = 2 * I / 128 * size_t(R) * 4; break;
         case MOE_TRAIN_ROW_GATE: *offset = W.row_gate; *bytes = size_t(R) * 4; break;
+        case MOE_TRAIN_LOGITS: *offset = W.logits; *bytes = size_t(T) * w->N * 4; break;
         default: return fail(MOE_ERR_INVALID_ARG, "moe_layer_train_buffer: unknown buffer %d", which);
     }
     return MOE_OK;
@@ -245,7 +248,7 @@ moe_status moe_layer_forward_train(const moe_layer_weights* w, const uint16_t* u
     o.topk_idx = nullptr;
     o.gates = nullptr;
     STATUS_OK(layer_forward(w, u, T, out, &o, update_bias, ws, W.fwd, stream, reinterpret_cast<float*>(ws + W.scores),
-                            reinterpret_cast<uint16_t*>(ws + W.H)));
+                            reinterpret_cast<uint16_t*>(ws + W.H), reinterpret_cast<float*>(ws + W.logits)));
     const size_t tk = size_t(T) * w->K;
     if (T > 0 && outs->topk_idx)
         CUDA_OK(cudaMemcpyAsync(outs->topk_idx, ws + W.fwd.topk, tk * 4, cudaMemcpyDeviceToDevice, stream));

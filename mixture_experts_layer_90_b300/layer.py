@@ -210,7 +210,7 @@ class MoELayer:
     def train_buffer(self, T: int, name: str) -> torch.Tensor:
         """A named buffer of the training workspace for T tokens (after
         forward_train / backward): H, scores, dg, dA, dH, dX, offsets,
-        perm_token, dest_row, y, kofs, dy_q, dy_s, dh_q, dh_s, row_gate."""
+        perm_token, dest_row, y, kofs, dy_q, dy_s, dh_q, dh_s, row_gate, logits."""
         off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
         _check(load_library().moe_layer_train_buffer(ctypes.byref(self._desc), T, TRAIN_BUFFERS[name],
                                                      ctypes.byref(off), ctypes.byref(nb)), "moe_layer_train_buffer")
@@ -223,7 +223,7 @@ class MoELayer:
             "dest_row": ((T, K), torch.int32), "y": ((R, d), torch.bfloat16), "kofs": ((N + 2,), torch.int32),
             "dy_q": ((R, d), torch.uint8), "dy_s": ((d // 128, R), torch.float32),
             "dh_q": ((R, 2 * I), torch.uint8), "dh_s": ((2 * I // 128, R), torch.float32),
-            "row_gate": ((R,), torch.float32),
+            "row_gate": ((R,), torch.float32), "logits": ((T, N), torch.float32),
         }[name]
         return raw.view(dtype).view(shape)
 

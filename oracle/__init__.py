@@ -466,7 +466,7 @@ class Backward:
 
 
 def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=1, topk_groups=1, fp8=True,
-                   route_all=None, stack=True) -> Backward:
+                   route_all=None, stack=True, wgrad_experts=None) -> Backward:
     """Gradient of L = sum(G * h') for the layer h' (nlp-lineage page, "The
     notation") with the expert choice held fixed (readings in moe_oracle.c,
     [train]):
@@ -476,7 +476,8 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
       expert e     dA = dY W2,  (dH1, dH3) = SwiGLU'(H1, H3) dA,  dX = dH1 W1 + dH3 W3
                    dW2 = dY^T A,  dW1 = dH1^T X,  dW3 = dH3^T X   (X = u of the rows)
       gates        with S = sum_k s_k and c = sum_k g_k dg_k:
-                   dz_{t,k} = (dg_{t,k} - c) / S * s_k (1 - s_k)
+                   dz_{t,k} = (dg_{t,k} - c) / S * s'(z_k), s'(z) = s (1 - s)
+                   = e^-|z| / (1 + e^-|z|)^2 from the logit z = u . e
       tokens       du_t = G_t + dX_shared,t + sum_k dX_{row(t,k)} + sum_k dz_{t,k} e_{idx}
       centroids    de_i = sum over (t,k) routed to i of dz_{t,k} u_t
 
@@ -498,7 +499,9 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
     expert_weights(e) -> (w1 [I,d], w3 [I,d], w2 [d,I]) as bf16 torch tensors or
     fp32 arrays; e = N is the shared expert; it is called only for experts
     with rows. stack=False returns dw1, dw3, dw2 as dicts over the experts
-    with rows (for samples of a large layer) instead of stacked arrays.
+    with rows (for samples of a large layer) instead of stacked arrays;
+    wgrad_experts (a set of expert ids, None = all) limits the weight
+    gradients to those experts (the others come out as zeros / absent).
     """
     import torch
     u_bits = as_bf16_bits(u_bf16)
@@ -559,6 +562,14 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
             qh1, sh1 = quant_1x128(bf16_round(dHt1))
             qh3, sh3 = quant_1x128(bf16_round(dHt3))
             dX = _bf(fp8_gemm(qh1, sh1, q1.T, s1.T) + fp8_gemm(qh3, sh3, q3.T, s3.T))
+            out.inter[e] = dict(Ht1=Ht1, Ht3=Ht3, Y=Y, dY=dY, dA=dA, dHt1=dHt1, dHt3=dHt3, dX=dX)
+            if wgrad_experts is not None and e not in wgrad_experts:
+                if e == N:
+                    Y_sh, dX_sh = Y, dX
+                else:
+                    Y_rows[rows] = Y
+                    dX_rows[rows] = dX
+                continue
             # weight gradients: operands quantised per (128 rows, column)
             A32 = _r32(swiglu(Ht1, Ht3))
             yq_t, ys_t = quant_128x1(dY)
@@ -569,7 +580,6 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
             dW2[e] = fp8_gemm_kscaled(yq_t, ys_t, aq_t, as_t)
             dW1[e] = fp8_gemm_kscaled(hq1_t, hs1_t, xq_t, xs_t)
             dW3[e] = fp8_gemm_kscaled(hq3_t, hs3_t, xq_t, xs_t)
-            out.inter[e] = dict(Ht1=Ht1, Ht3=Ht3, Y=Y, dY=dY, dA=dA, dHt1=dHt1, dHt3=dHt3, dX=dX)
         else:
             W1, W3, W2 = (w.astype(np.float64) for w in (w1, w3, w2))
             H1, H3 = X @ W1.T, X @ W3.T
@@ -579,9 +589,10 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
             dA = dY @ W2
             dH1, dH3 = swiglu_backward(H1, H3, dA)
             dX = dH1 @ W1 + dH3 @ W3
-            dW2[e] = dY.T @ A
-            dW1[e] = dH1.T @ X
-            dW3[e] = dH3.T @ X
+            if wgrad_experts is None or e in wgrad_experts:
+                dW2[e] = dY.T @ A
+                dW1[e] = dH1.T @ X
+                dW3[e] = dH3.T @ X
             out.inter[e] = dict(Ht1=H1, Ht3=H3, Y=Y, dY=dY, dA=dA, dHt1=dH1, dHt3=dH3, dX=dX)
         if e == N:
             Y_sh, dX_sh = Y, dX
@@ -595,7 +606,10 @@ def layer_backward(u_bf16, centroids, bias, K, expert_weights, G_bf16, n_groups=
     s_sel = np.take_along_axis(s, idx.astype(np.int64), axis=1)
     S = s_sel.sum(axis=1, keepdims=True)
     c = (g * dg).sum(axis=1, keepdims=True)
-    dz = (dg - c) / S * s_sel * (1.0 - s_sel)
+    # the sigmoid's derivative s (1 - s), from the logit z = u . e (no cancellation near s = 1)
+    z = np.einsum("td,tkd->tk", uv, Ev[idx])
+    ez = np.exp(-np.abs(z))
+    dz = (dg - c) / S * (ez / (1.0 + ez) ** 2)
     du = Gv + dX_sh + dX_rows[rows_tk].sum(axis=1) + np.einsum("tk,tkd->td", dz, Ev[idx])
     de = np.zeros((N, d))
     for i in range(N):
