@@ -26,6 +26,7 @@ workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import itertools
 import json
 import math
 import os
@@ -800,6 +801,29 @@ def case_gemm_slice(moe, S, dev, args, flush, which):
             "l2": "flushed before each launch"}
 
 
+def case_wgrad_slice(moe, S, dev, args, flush):
+    """The backward's dW13 GEMM for 16 experts of the V3 shape (fp32 [16, 4096,
+    7168] out, 2-3 blocks of 128 tokens per expert, seeded codes and scales):
+    a small case for profiling the weight-gradient mode."""
+    import torch
+    G, M, Nd = 16, 4096, 7168
+    blocks = [2 + (e * 7) % 2 for e in range(G)]
+    kofs = torch.tensor([0] + list(itertools.accumulate(blocks)), dtype=torch.int32, device=dev)
+    Kp = int(kofs[-1].item()) * 128
+    key = S.key(0, "wgrad-slice", G, M, Nd)
+    A = (S.bits(key, 0, M * Kp, dev) % 120).to(torch.uint8).view(M, Kp)
+    B = (S.bits(key, M * Kp, Nd * Kp, dev) % 120).to(torch.uint8).view(Nd, Kp)
+    sa = S.uniform((Kp // 128, M), 0.5, 1.5, S.key(1, "wgrad-slice-sa"), dev)
+    sb = S.uniform((Kp // 128, Nd), 0.5, 1.5, S.key(1, "wgrad-slice-sb"), dev)
+    C = torch.empty((G, M, Nd), dtype=torch.float32, device=dev)
+    ms = time_launches(lambda: moe.fp8_grouped_gemm_wgrad(A, sa, B, sb, kofs, out=C), args.steps, args.warmup, flush)
+    pk, src = peaks()
+    out_gb = C.numel() * 4 / 1e9
+    return {"workload": f"wgrad-fp8-{G}x{M}x{Nd}-k{Kp}", "ms": ms, "out_gbs": out_gb / ms * 1e3,
+            "frac_of_hbm": out_gb / ms * 1e3 / pk["hbm_gbs"], "peak_source": f"{src} hbm copy",
+            "l2": "flushed before each launch"}
+
+
 def run_case(args):
     import torch
 
@@ -822,6 +846,8 @@ def run_case(args):
         line.update(case_dispatch(moe, S, dev, args, flush, args.case))
     elif args.case == "train":
         line.update(case_train(moe, S, dev, args, flush, cpu_baseline=cb))
+    elif args.case == "wgrad-small":
+        line.update(case_wgrad_slice(moe, S, dev, args, flush))
     elif args.case in ("decode64", "decode256"):
         sh = S.LAYER_V3
         cent = S.centroids(sh, zipf=True).to(dev)
@@ -844,7 +870,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="time the V3 layer only")
     ap.add_argument("--case", default="layer",
                     choices=["layer", "tiny", "route", "gemm", "gemm1-small", "gemm2-small", "decode64",
-                             "decode256", "permute-fp8", "combine", "train"],
+                             "decode256", "permute-fp8", "combine", "train", "wgrad-small"],
                     help="layer: the V3 layer step with every other workload (the benchmark line); the others "
                          "time one workload alone")
     args = ap.parse_args()
