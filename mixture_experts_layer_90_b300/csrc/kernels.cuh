@@ -56,7 +56,9 @@ cudaError_t launch_combine_bwd(const uint16_t* G, const uint16_t* y, const float
 cudaError_t launch_swiglu_bwd(const uint16_t* dA, const uint16_t* H, int64_t R, int I, uint16_t* dH, uint8_t* qdh,
                               float* sdh, cudaStream_t stream);
 cudaError_t launch_kblock_offsets(const int32_t* offsets, int G, int32_t* kofs, cudaStream_t stream);
-cudaError_t launch_quant_t(int src_kind, const int32_t* offsets, const int32_t* kofs, int G, int64_t TK,
+cudaError_t launch_pad_rows(const int32_t* offsets, const int32_t* kofs, int G, int64_t Kp, int32_t* prow,
+                            cudaStream_t stream);
+cudaError_t launch_quant_t(int src_kind, const int32_t* prow, const int32_t* kofs, int G, int64_t TK,
                            const int32_t* perm_token, const float* row_gate, const uint16_t* src, int C,
                            int64_t Kp, uint8_t* q, float* s, cudaStream_t stream);
 cudaError_t launch_unpermute_bwd(const uint16_t* G, const uint16_t* dX, const int32_t* dest, const int32_t* topk,

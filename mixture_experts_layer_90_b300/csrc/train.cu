@@ -8,7 +8,7 @@ namespace {
 // The training workspace: the forward's (LayerWs), then the buffers below.
 struct TrainWs {
     LayerWs fwd;
-    size_t H, scores, logits, row_gate, dg, qdy, sdy, dA, dH, qdh, sdh, dX, kofs, dz_row;
+    size_t H, scores, logits, row_gate, dg, qdy, sdy, dA, dH, qdh, sdh, dX, kofs, dz_row, prow;
     size_t qyt, syt, qat, sat, qht, sht, qxt, sxt;
     int64_t Kp;   // padded token rows of the weight-gradient operands
     size_t total;
@@ -43,6 +43,7 @@ TrainWs train_ws(const moe_layer_weights* w, int64_t T) {
     W.kofs = take(size_t(G + 1) * 4);
     W.dz_row = take(size_t(T) * w->K * 4);
     const size_t Kp = size_t(W.Kp), nkb = Kp / 128;
+    W.prow = take(Kp * 4);
     W.qyt = take(d * Kp);
     W.syt = take(nkb * d * 4);
     W.qat = take(I * Kp);
@@ -158,6 +159,8 @@ moe_status layer_backward(const moe_layer_weights* w, const moe_layer_weights_t*
     // weight gradients: operands per (128 tokens of an expert, column), transposed
     CUDA_OK(moe::launch_kblock_offsets(offsets, G, kofs, stream));
     const int64_t Kp = W.Kp, TK = T * K;
+    int32_t* prow = reinterpret_cast<int32_t*>(ws + W.prow);
+    CUDA_OK(moe::launch_pad_rows(offsets, kofs, G, Kp, prow, stream));
     uint8_t* qyt = ws + W.qyt;
     uint8_t* qat = ws + W.qat;
     uint8_t* qht = ws + W.qht;
@@ -166,13 +169,13 @@ moe_status layer_backward(const moe_layer_weights* w, const moe_layer_weights_t*
     float* sat = reinterpret_cast<float*>(ws + W.sat);
     float* sht = reinterpret_cast<float*>(ws + W.sht);
     float* sxt = reinterpret_cast<float*>(ws + W.sxt);
-    CUDA_OK(moe::launch_quant_t(moe::kQuantTScaledG, offsets, kofs, G, TK, perm_token, row_gate, dout, d, Kp, qyt,
+    CUDA_OK(moe::launch_quant_t(moe::kQuantTScaledG, prow, kofs, G, TK, perm_token, row_gate, dout, d, Kp, qyt,
                                 syt, stream));
-    CUDA_OK(moe::launch_quant_t(moe::kQuantTSwiglu, offsets, kofs, G, TK, perm_token, nullptr, H, I, Kp, qat, sat,
+    CUDA_OK(moe::launch_quant_t(moe::kQuantTSwiglu, prow, kofs, G, TK, perm_token, nullptr, H, I, Kp, qat, sat,
                                 stream));
-    CUDA_OK(moe::launch_quant_t(moe::kQuantTRows, offsets, kofs, G, TK, perm_token, nullptr, dH, 2 * I, Kp, qht, sht,
+    CUDA_OK(moe::launch_quant_t(moe::kQuantTRows, prow, kofs, G, TK, perm_token, nullptr, dH, 2 * I, Kp, qht, sht,
                                 stream));
-    CUDA_OK(moe::launch_quant_t(moe::kQuantTTokens, offsets, kofs, G, TK, perm_token, nullptr, u, d, Kp, qxt, sxt,
+    CUDA_OK(moe::launch_quant_t(moe::kQuantTTokens, prow, kofs, G, TK, perm_token, nullptr, u, d, Kp, qxt, sxt,
                                 stream));
     STATUS_OK(mark(6));
     // dW2 = dY^T A  [G][d][I];  dW13 = dH^T X  [G][2I][d]
