@@ -441,8 +441,10 @@ __global__ void __launch_bounds__(256) fp8_transpose_kernel(const uint8_t* __res
 // stored row-major (q, s [G][rows/128][cols/128]) and transposed (qt [G][cols][rows],
 // st [G][cols/128][rows/128]). Warp w takes rows 16w..16w+15 of the block and
 // lane l columns 4l..4l+3, so every load and store of a warp covers one whole
-// 512-byte row of the block.
-__global__ void __launch_bounds__(256) sgd_requant_kernel(float* __restrict__ w, const float* __restrict__ grad,
+// 512-byte row of the block. The first pass updates the master and takes the
+// amax; the second reads the new values back (from L2) to quantise them, so a
+// thread never holds more than 4 rows (more blocks per SM, more loads in flight).
+__global__ void __launch_bounds__(256, 4) sgd_requant_kernel(float* __restrict__ w, const float* __restrict__ grad,
                                                           int rows, int cols, float lr, uint8_t* __restrict__ q,
                                                           float* __restrict__ s, uint8_t* __restrict__ qt,
                                                           float* __restrict__ st) {
@@ -452,21 +454,27 @@ __global__ void __launch_bounds__(256) sgd_requant_kernel(float* __restrict__ w,
     const int64_t g = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
     const int64_t base = g * int64_t(rows) * cols + int64_t(br * 128 + 16 * wp) * cols + bc * 128 + 4 * lane;
-    float4 x[16];
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int64_t off = base + int64_t(i) * cols;
-        float4 v = *reinterpret_cast<const float4*>(w + off);
-        const float4 d = __ldg(reinterpret_cast<const float4*>(grad + off));
-        // two fp32 roundings, never fused: the product, then the difference
-        v.x = __fsub_rn(v.x, __fmul_rn(lr, d.x));
-        v.y = __fsub_rn(v.y, __fmul_rn(lr, d.y));
-        v.z = __fsub_rn(v.z, __fmul_rn(lr, d.z));
-        v.w = __fsub_rn(v.w, __fmul_rn(lr, d.w));
-        *reinterpret_cast<float4*>(w + off) = v;
-        x[i] = v;
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    for (int i0 = 0; i0 < 16; i0 += 4) {
+        float4 v[4];
+        float4 d[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t off = base + int64_t(i0 + i) * cols;
+            v[i] = *reinterpret_cast<const float4*>(w + off);
+            d[i] = __ldg(reinterpret_cast<const float4*>(grad + off));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // two fp32 roundings, never fused: the product, then the difference
+            v[i].x = __fsub_rn(v[i].x, __fmul_rn(lr, d[i].x));
+            v[i].y = __fsub_rn(v[i].y, __fmul_rn(lr, d[i].y));
+            v[i].z = __fsub_rn(v[i].z, __fmul_rn(lr, d[i].z));
+            v[i].w = __fsub_rn(v[i].w, __fmul_rn(lr, d[i].w));
+            *reinterpret_cast<float4*>(w + base + int64_t(i0 + i) * cols) = v[i];
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -477,11 +485,17 @@ __global__ void __launch_bounds__(256) sgd_requant_kernel(float* __restrict__ w,
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, warp_max[i]);
     const float sc = tile_scale(amax);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t c = pack_e4m3x2(__fdiv_rn(x[i].x, sc), __fdiv_rn(x[i].y, sc)) |
-                           (pack_e4m3x2(__fdiv_rn(x[i].z, sc), __fdiv_rn(x[i].w, sc)) << 16);
-        *reinterpret_cast<uint32_t*>(q + base + int64_t(i) * cols) = c;
-        *reinterpret_cast<uint32_t*>(&tile[16 * wp + i][4 * lane]) = c;
+    for (int i0 = 0; i0 < 16; i0 += 4) {
+        float4 x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = *reinterpret_cast<const float4*>(w + base + int64_t(i0 + i) * cols);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t c = pack_e4m3x2(__fdiv_rn(x[i].x, sc), __fdiv_rn(x[i].y, sc)) |
+                               (pack_e4m3x2(__fdiv_rn(x[i].z, sc), __fdiv_rn(x[i].w, sc)) << 16);
+            *reinterpret_cast<uint32_t*>(q + base + int64_t(i0 + i) * cols) = c;
+            *reinterpret_cast<uint32_t*>(&tile[16 * wp + i0 + i][4 * lane]) = c;
+        }
     }
     __syncthreads();
     // transposed: 8 lanes per output row of 128 bytes (16 each), 32 rows per pass
