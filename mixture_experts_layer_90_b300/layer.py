@@ -265,6 +265,22 @@ class MoELayer:
                                                  _stream()), "moe_layer_backward")
         return du
 
+    def capture_train(self, u: torch.Tensor, dout: torch.Tensor, lr: float, out: torch.Tensor = None,
+                      du: torch.Tensor = None) -> "TrainGraph":
+        """Records one training step on the static buffers u, dout -> out, du
+        into a CUDA graph (learning rate fixed at capture). A training forward
+        and backward run first, outside the capture, with no update (no bias
+        move, no SGD), so that per-device set-up and the workspace exist."""
+        out = torch.empty_like(u) if out is None else out
+        du = torch.empty_like(u) if du is None else du
+        self.forward_train(u, out, update_bias=False)
+        self.backward(u, dout, du)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.train_step(u, dout, lr, out, du)
+        return TrainGraph(g, u, dout, out, du, self)
+
     def train_step(self, u: torch.Tensor, dout: torch.Tensor, lr: float, out: torch.Tensor = None,
                    du: torch.Tensor = None):
         """One SGD step (forward_train with the bias update, backward, SGD on the
@@ -280,6 +296,19 @@ class MoELayer:
                                                    _p(out), _p(du), ctypes.byref(outs), ctypes.byref(grads), _p(ws),
                                                    ws.numel(), _stream()), "moe_layer_train_step")
         return out, du
+
+
+class TrainGraph:
+    """A captured training step: copy a batch into `u` and its dL/dh' into
+    `dout`, call replay(); `out`, `du` and the layer's weights, bias and
+    centroids then hold the step's results."""
+
+    def __init__(self, graph, u, dout, out, du, layer):
+        self.graph, self.u, self.dout, self.out, self.du, self.layer = graph, u, dout, out, du, layer
+
+    def replay(self):
+        self.graph.replay()
+        return self.out, self.du
 
 
 class LayerGraph:

@@ -318,3 +318,30 @@ def test_training_steps_match_the_oracle():
         x = w / sc
         assert np.all(np.abs(vals[q] - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10) * 1.0000001)
         np.testing.assert_array_equal(layer.w2t[e].cpu().numpy(), q.T)
+
+
+def test_training_step_graph_replay_matches_eager():
+    """The training step captured in a CUDA graph and replayed on two batches
+    leaves the same bits as two eager steps: h', du, masters, FP8 weights and
+    their transposed copies, scales, centroids, bias."""
+    m = _lib()
+    sh = S.LayerShape(T=128, d=256, N=8, K=2, I=256, name="train-graph")
+    eager, graphed = _build(sh), _build(sh)
+    lr = 1e-3
+    u = torch.empty((sh.T, sh.d), dtype=torch.bfloat16, device="cuda")
+    G = torch.empty_like(u)
+    g = graphed.capture_train(u, G, lr)
+    for step in range(2):
+        ub, Gb = S.tokens(sh, seed=50 + step).cuda(), S.grad_out(sh, seed=60 + step).cuda()
+        out_e, du_e = eager.train_step(ub, Gb, lr)
+        u.copy_(ub)
+        G.copy_(Gb)
+        out_g, du_g = g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g.view(torch.int16), out_e.view(torch.int16)), step
+        assert torch.equal(du_g.view(torch.int16), du_e.view(torch.int16)), step
+        for name in ("w13_master", "w2_master", "w13", "w13_scales", "w2", "w2_scales", "w13t", "w2t", "centroids",
+                     "bias"):
+            a, b = getattr(graphed, name), getattr(eager, name)
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (step, name)
+    assert m.device_status() == 0
