@@ -8,6 +8,9 @@
 //   scan    per expert: exclusive prefix over chunks, and the expert total
 //   rank    warp per chunk: row = offsets[e] + prefix + rank among equal
 //           experts in (token, k) order (__match_any_sync)
+//   small   batches of at most 8192 pairs over at most 256 experts: count,
+//           scan and rank in one block (one launch instead of three; the
+//           decode and small layers are bound by dependent launches)
 //   scatter warp per token: the token's row is read once and written to its K
 //           rows (and to the shared expert's row), optionally quantised to
 //           E4M3 per 1x128 tile on the way.
@@ -95,6 +98,33 @@ __device__ void block_offsets(const int32_t* totals, int N, int* off_sm) {
     __syncthreads();
 }
 
+// Rows of the pairs [p0, p1), walked 32 at a time by one warp: run[e] holds
+// the next row of expert e and advances past this group's pairs of e.
+__device__ void rank_pairs(const int32_t* __restrict__ idx, int64_t p0, int64_t p1, int N, int K, int* run,
+                           int32_t* __restrict__ perm_token, int32_t* __restrict__ dest_row) {
+    const int lane = threadIdx.x & 31;
+    for (int64_t pb = p0; pb < p1; pb += 32) {
+        const int64_t p = pb + lane;
+        const bool active = p < p1;
+        int e = active ? __ldg(idx + p) : -1 - lane;
+        if (e < 0 || e >= N) {
+            // out of range (reported by the count pass): the pair gets no row
+            if (active) dest_row[p] = -1;
+            e = -1 - lane;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        if (active && e >= 0) {
+            const int before = __popc(peers & ((1u << lane) - 1u));
+            const int row = run[e] + before;
+            dest_row[p] = row;
+            perm_token[row] = int32_t(p / K);
+        }
+        __syncwarp();
+        if (active && e >= 0 && (peers & ((1u << lane) - 1u)) == 0) run[e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
 __global__ void __launch_bounds__(256) perm_rank_kernel(const int32_t* __restrict__ idx, int64_t T, int N, int K,
                                                         const int32_t* __restrict__ prefix,
                                                         const int32_t* __restrict__ totals, int with_shared,
@@ -114,28 +144,52 @@ __global__ void __launch_bounds__(256) perm_rank_kernel(const int32_t* __restric
     for (int64_t c = int64_t(blockIdx.x) * 8 + w; c < n_chunks; c += int64_t(gridDim.x) * 8) {
         for (int i = lane; i < N; i += 32) run[i] = off_sm[i] + prefix[c * N + i];
         __syncwarp();
-        const int64_t p0 = c * kChunk * K, p1 = min(T, (c + 1) * kChunk) * K;
-        for (int64_t pb = p0; pb < p1; pb += 32) {
-            const int64_t p = pb + lane;
-            const bool active = p < p1;
-            int e = active ? __ldg(idx + p) : -1 - lane;
-            if (e < 0 || e >= N) {
-                // out of range (reported by the count pass): the pair gets no row
-                if (active) dest_row[p] = -1;
-                e = -1 - lane;
-            }
-            const uint32_t peers = __match_any_sync(0xffffffffu, e);
-            if (active && e >= 0) {
-                const int before = __popc(peers & ((1u << lane) - 1u));
-                const int row = run[e] + before;
-                dest_row[p] = row;
-                perm_token[row] = int32_t(p / K);
-            }
-            __syncwarp();
-            if (active && e >= 0 && (peers & ((1u << lane) - 1u)) == 0) run[e] += __popc(peers);
-            __syncwarp();
-        }
+        rank_pairs(idx, c * kChunk * K, min(T, (c + 1) * kChunk) * K, N, K, run, perm_token, dest_row);
     }
+}
+
+// Count, scan and rank of a small batch in one block of 32 warps. Warp w owns
+// the contiguous pair range [w*L, (w+1)*L), so an expert's rows still come in
+// (token, k) order: warps in order, and lanes in order within a warp.
+constexpr int64_t kSmallPairs = 8192;
+constexpr int kSmallMaxN = 256;
+
+__global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restrict__ idx, int64_t T, int N, int K,
+                                                          int with_shared, int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ perm_token,
+                                                          int32_t* __restrict__ dest_row) {
+    extern __shared__ int sh[];
+    int* off_sm = sh;            // [N+1]
+    int* tot = sh + N + 1;       // [N]
+    int* hist = tot + N;         // [32][N]: warp w's counts, then its next row per expert
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t P = T * K, L = (P + 31) / 32;
+    const int64_t p0 = min(P, int64_t(w) * L), p1 = min(P, int64_t(w + 1) * L);
+    for (int i = threadIdx.x; i < 32 * N; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    int* h = hist + w * N;
+    for (int64_t p = p0 + lane; p < p1; p += 32) {
+        const int e = __ldg(idx + p);
+        if (e >= 0 && e < N) atomicAdd(&h[e], 1);
+        else report(MOE_ERR_DEVICE_DATA);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        int run = 0;
+        for (int v = 0; v < 32; ++v) {
+            const int c = hist[v * N + e];
+            hist[v * N + e] = run;
+            run += c;
+        }
+        tot[e] = run;
+    }
+    __syncthreads();
+    block_offsets(tot, N, off_sm);
+    for (int i = threadIdx.x; i <= N; i += blockDim.x) offsets[i] = off_sm[i];
+    if (with_shared && threadIdx.x == 0) offsets[N + 1] = off_sm[N] + int32_t(T);
+    for (int i = lane; i < N; i += 32) h[i] += off_sm[i];
+    __syncwarp();
+    rank_pairs(idx, p0, p1, N, K, h, perm_token, dest_row);
 }
 
 // Token-major scatter of rows (bf16 copy or E4M3 1x128 quantisation). A warp
@@ -228,15 +282,19 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
             return e;
         return cudaSuccess;
     }
-    {
-        int64_t blocks = (n_chunks + 7) / 8;
-        if (blocks > cap) blocks = cap;
-        perm_count_kernel<<<int(blocks), 256, size_t(8) * N * 4, stream>>>(topk_idx, T, N, K, counts);
+    if (T * K <= kSmallPairs && N <= kSmallMaxN) {
+        perm_small_kernel<<<1, 1024, size_t(34 * N + 1) * 4, stream>>>(topk_idx, T, N, K, with_shared, offsets,
+                                                                       perm_token, dest_row);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    perm_scan_kernel<<<(N + 31) / 32, 1024, 0, stream>>>(counts, n_chunks, N, totals);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    {
+    } else {
+        {
+            int64_t blocks = (n_chunks + 7) / 8;
+            if (blocks > cap) blocks = cap;
+            perm_count_kernel<<<int(blocks), 256, size_t(8) * N * 4, stream>>>(topk_idx, T, N, K, counts);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        perm_scan_kernel<<<(N + 31) / 32, 1024, 0, stream>>>(counts, n_chunks, N, totals);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
         int64_t blocks = (n_chunks + 7) / 8;
         if (blocks > cap) blocks = cap;
         const size_t smem = size_t(N + 1) * 4 + size_t(8) * N * 4;

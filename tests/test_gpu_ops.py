@@ -331,7 +331,12 @@ def _rand_topk(T, N, K, seed=0):
                                                  (333, 640, 256, 8, True, True), (64, 256, 1024, 16, True, False),
                                                  # widths that leave part of the warp's 512-column step idle
                                                  (77, 384, 8, 3, False, True), (129, 896, 64, 6, False, False),
-                                                 (50, 128, 4, 2, True, True), (91, 1152, 32, 5, True, False)])
+                                                 (50, 128, 4, 2, True, True), (91, 1152, 32, 5, True, False),
+                                                 # either side of the single-block path's limit (8192 pairs,
+                                                 # 256 experts): the last one-block batch, then ragged
+                                                 # multi-block batches just past the pair and expert limits
+                                                 (1024, 256, 256, 8, True, True), (1025, 256, 256, 8, False, True),
+                                                 (1500, 128, 32, 6, False, False), (100, 128, 257, 8, True, True)])
 def test_permute_bit_exact(T, d, N, K, fp8, shared):
     x = bf16((T, d), 1.0, "px", T, d)
     idx = _rand_topk(T, N, K)
