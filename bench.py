@@ -453,11 +453,12 @@ def case_tiny(moe, S, dev, args, flush, cpu_baseline=True):
     pk, src = peaks()
     res = {"workload": "tiny-bf16-layer T=128 d=256 16+1 experts top-4 I=128", "ms": ms, "us_per_layer": 1e3 * ms,
            "us_per_layer_eager": 1e3 * ms_eager, "tokens_per_s": sh.T / ms * 1e3, "dtype": "bf16",
-           # loads memset, gate GEMM, select | one-block count/scan/rank, scatter | GEMM1 | GEMM2 | combine
-           "launches": 8, "timing": "CUDA-graph replay of the layer call (eager call beside it)",
+           # gate GEMM, select | one-block count/scan/rank (it also writes the loads), scatter | GEMM1 | GEMM2 |
+           # combine
+           "launches": 7, "timing": "CUDA-graph replay of the layer call (eager call beside it)",
            "roofline": {"bound": "tensor", "achieved": flop / ms / 1e9, "peak": pk["bf16_tflops"],
                         "unit": "TFLOP/s", "frac": flop / ms / 1e9 / pk["bf16_tflops"], "traffic": None,
-                        "note": "launch-latency bound: 7 dependent kernels and a memset, a few microseconds each",
+                        "note": "launch-latency bound: 7 dependent kernels of a few microseconds each",
                         "peak_source": f"{src} bf16 burst"}}
     if cpu_baseline:
         w = {e: S.expert_weights(sh, e) for e in range(sh.N + 1)}

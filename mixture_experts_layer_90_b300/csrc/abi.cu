@@ -78,7 +78,6 @@ moe_status check_route(const uint16_t* u, int64_t T, int d, const void* centroid
         REQUIRE(topk_groups >= 1 && topk_groups <= n_groups, "moe_route: topk_groups=%d", topk_groups);
         REQUIRE(topk_groups * (N / n_groups) >= K, "moe_route: kept groups hold fewer than K experts");
     }
-    REQUIRE(loads, "moe_route: null loads");
     if (T == 0) return MOE_OK;   // no token: only the loads are written (zero)
     REQUIRE(u && centroids && bias && idx && gates, "moe_route: null pointer");
     REQUIRE(al16(u) && al16(centroids), "moe_route: u and centroids must be 16-byte aligned");
@@ -177,6 +176,7 @@ moe_status moe_route_prepared(const uint16_t* u, int64_t T, int d, const void* p
                               const float* bias, int N, int K, int n_groups, int topk_groups, int32_t* topk_idx,
                               float* gates, int32_t* loads, float* scores, void* workspace, size_t workspace_bytes,
                               moe_stream_t stream) {
+    REQUIRE(loads, "moe_route: null loads");
     return route_prepared_impl(u, T, d, prepared, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates,
                                loads, scores, workspace, workspace_bytes, stream, nullptr);
 }
@@ -200,6 +200,7 @@ static moe_status route_impl(const uint16_t* u, int64_t T, int d, const void* ce
 moe_status moe_route(const uint16_t* u, int64_t T, int d, const void* centroids, int centroid_dtype, const float* bias,
                      int N, int K, int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
                      float* scores, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    REQUIRE(loads, "moe_route: null loads");
     return route_impl(u, T, d, centroids, centroid_dtype, bias, N, K, n_groups, topk_groups, topk_idx, gates, loads,
                       scores, workspace, workspace_bytes, stream, nullptr);
 }
@@ -228,9 +229,12 @@ moe_status moe_route_balance_stats(const float* scores, const int32_t* topk_idx,
 
 size_t moe_permute_workspace_size(int64_t T, int N) { return moe::permute_ws_bytes(T, N); }
 
-moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K, int out_dtype,
-                       int with_shared, int32_t* offsets, int32_t* perm_token, int32_t* dest_row, void* x_perm,
-                       float* x_perm_scales, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+// loads (internal, may be null): the per-expert pair counts, written by the permutation
+// (the layer takes its loads from here instead of from the routing)
+static moe_status permute_impl(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K,
+                               int out_dtype, int with_shared, int32_t* offsets, int32_t* perm_token, int32_t* dest_row,
+                               void* x_perm, float* x_perm_scales, void* workspace, size_t workspace_bytes,
+                               moe_stream_t stream, int32_t* loads) {
     REQUIRE(T >= 0 && T * (K + 1) <= kMaxRows, "moe_permute: T=%lld out of range", (long long)T);
     REQUIRE(d > 0 && d % 128 == 0, "moe_permute: d=%d must be a multiple of 128", d);
     REQUIRE(N >= 1 && N <= 1024, "moe_permute: N=%d must be in [1, 1024]", N);
@@ -246,8 +250,15 @@ moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return fail(MOE_ERR_WORKSPACE, "moe_permute: workspace needs %zu bytes", need);
     CUDA_OK(moe::launch_permute(x, T, d, topk_idx, N, K, out_dtype, with_shared ? 1 : 0, offsets, perm_token,
-                                dest_row, x_perm, x_perm_scales, workspace, stream));
+                                dest_row, x_perm, x_perm_scales, workspace, stream, loads));
     return MOE_OK;
+}
+
+moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K, int out_dtype,
+                       int with_shared, int32_t* offsets, int32_t* perm_token, int32_t* dest_row, void* x_perm,
+                       float* x_perm_scales, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    return permute_impl(x, T, d, topk_idx, N, K, out_dtype, with_shared, offsets, perm_token, dest_row, x_perm,
+                        x_perm_scales, workspace, workspace_bytes, stream, nullptr);
 }
 
 // fp8_grouped_gemm; with h_out (MOE_EPI_SWIGLU_FP8 only) the products are also
@@ -448,17 +459,18 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
         return MOE_OK;
     };
     STATUS_OK(mark(0));
+    // the routing leaves the loads to the permutation, which counts the pairs per expert anyway
     if (w->centroids_prepared)
         STATUS_OK(route_prepared_impl(u, T, d, w->centroids_prepared, w->centroid_dtype, w->bias, N, K, w->n_groups,
-                                      w->topk_groups, topk, gates, loads, scores, ws + L.route, L.perm - L.route,
+                                      w->topk_groups, topk, gates, nullptr, scores, ws + L.route, L.perm - L.route,
                                       stream, logits));
     else
         STATUS_OK(route_impl(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups,
-                             topk, gates, loads, scores, ws + L.route, L.perm - L.route, stream, logits));
+                             topk, gates, nullptr, scores, ws + L.route, L.perm - L.route, stream, logits));
     STATUS_OK(mark(1));
-    STATUS_OK(moe_permute(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
-                          reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,
-                          reinterpret_cast<float*>(ws + L.x_scales), ws + L.perm, L.offsets - L.perm, stream));
+    STATUS_OK(permute_impl(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
+                           reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,
+                           reinterpret_cast<float*>(ws + L.x_scales), ws + L.perm, L.offsets - L.perm, stream, loads));
     STATUS_OK(mark(2));
     if (w->fp8) {
         STATUS_OK(fp8_gemm_impl(ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales),

@@ -36,7 +36,7 @@ cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* prepar
 size_t permute_ws_bytes(int64_t T, int N);
 cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K, int out_dtype,
                            int with_shared, int32_t* offsets, int32_t* perm_token, int32_t* dest_row, void* x_perm,
-                           float* x_perm_scales, void* ws, cudaStream_t stream);
+                           float* x_perm_scales, void* ws, cudaStream_t stream, int32_t* loads = nullptr);
 
 // Sequence-wise balance statistics (balance.cu).
 size_t balance_ws_bytes(int64_t T, int N, int64_t seq_len);

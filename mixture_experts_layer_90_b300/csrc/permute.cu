@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(256) perm_count_kernel(const int32_t* __restri
 
 // Block b handles experts 32b..32b+31; warp s of it handles chunk segment s.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ counts, int64_t n_chunks, int N,
-                                                         int32_t* __restrict__ totals) {
+                                                         int32_t* __restrict__ totals, int32_t* __restrict__ loads) {
     __shared__ int part[32][33];
     const int lane = threadIdx.x & 31, seg = threadIdx.x >> 5;
     const int e = blockIdx.x * 32 + lane;
@@ -66,7 +66,10 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
             counts[c * N + e] = run;
             run += v;
         }
-        if (seg == 31) totals[e] = run;
+        if (seg == 31) {
+            totals[e] = run;
+            if (loads) loads[e] = run;
+        }
     }
 }
 
@@ -157,7 +160,8 @@ constexpr int kSmallMaxN = 256;
 __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restrict__ idx, int64_t T, int N, int K,
                                                           int with_shared, int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ perm_token,
-                                                          int32_t* __restrict__ dest_row) {
+                                                          int32_t* __restrict__ dest_row,
+                                                          int32_t* __restrict__ loads) {
     extern __shared__ int sh[];
     int* off_sm = sh;            // [N+1]
     int* tot = sh + N + 1;       // [N]
@@ -182,6 +186,7 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
             run += c;
         }
         tot[e] = run;
+        if (loads) loads[e] = run;
     }
     __syncthreads();
     block_offsets(tot, N, off_sm);
@@ -271,7 +276,7 @@ size_t permute_ws_bytes(int64_t T, int N) {
 
 cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_idx, int N, int K, int out_dtype,
                            int with_shared, int32_t* offsets, int32_t* perm_token, int32_t* dest_row, void* x_perm,
-                           float* x_perm_scales, void* ws, cudaStream_t stream) {
+                           float* x_perm_scales, void* ws, cudaStream_t stream, int32_t* loads) {
     const int64_t n_chunks = (T + kChunk - 1) / kChunk;
     int32_t* counts = reinterpret_cast<int32_t*>(ws);
     int32_t* totals = counts + n_chunks * N;
@@ -280,11 +285,11 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
     if (T == 0) {
         if ((e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (N + 1 + (with_shared ? 1 : 0)), stream)) != cudaSuccess)
             return e;
-        return cudaSuccess;
+        return loads ? cudaMemsetAsync(loads, 0, sizeof(int32_t) * N, stream) : cudaSuccess;
     }
     if (T * K <= kSmallPairs && N <= kSmallMaxN) {
         perm_small_kernel<<<1, 1024, size_t(34 * N + 1) * 4, stream>>>(topk_idx, T, N, K, with_shared, offsets,
-                                                                       perm_token, dest_row);
+                                                                       perm_token, dest_row, loads);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     } else {
         {
@@ -293,7 +298,7 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
             perm_count_kernel<<<int(blocks), 256, size_t(8) * N * 4, stream>>>(topk_idx, T, N, K, counts);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        perm_scan_kernel<<<(N + 31) / 32, 1024, 0, stream>>>(counts, n_chunks, N, totals);
+        perm_scan_kernel<<<(N + 31) / 32, 1024, 0, stream>>>(counts, n_chunks, N, totals, loads);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         int64_t blocks = (n_chunks + 7) / 8;
         if (blocks > cap) blocks = cap;

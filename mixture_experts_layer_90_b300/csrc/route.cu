@@ -210,8 +210,9 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < N; i += blockDim.x)
-        if (hist[i]) atomicAdd(loads + i, hist[i]);
+    if (loads)
+        for (int i = threadIdx.x; i < N; i += blockDim.x)
+            if (hist[i]) atomicAdd(loads + i, hist[i]);
 }
 
 template <int J>
@@ -285,7 +286,8 @@ cudaError_t launch_route_prepare(const void* centroids, int centroid_dtype, int 
 cudaError_t launch_route(const uint16_t* u, int64_t T, int d, const void* prepared, const float* bias, int N, int K,
                          int n_groups, int topk_groups, int32_t* topk_idx, float* gates, int32_t* loads,
                          float* scores, void* zpart_ws, const RoutePlan& plan, cudaStream_t stream, float* logits) {
-    cudaError_t e = cudaMemsetAsync(loads, 0, sizeof(int32_t) * N, stream);
+    // loads may be null: the caller counts them elsewhere (the layer's permutation does)
+    cudaError_t e = loads ? cudaMemsetAsync(loads, 0, sizeof(int32_t) * N, stream) : cudaSuccess;
     if (e != cudaSuccess || T == 0) return e;
     const uint16_t* esplit = reinterpret_cast<const uint16_t*>(prepared);
     float* zpart = reinterpret_cast<float*>(zpart_ws);
