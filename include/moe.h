@@ -300,8 +300,9 @@ size_t moe_layer_workspace_size(const moe_layer_weights* w, int64_t T);
 
 /* h' for T tokens: u bf16 [T, d] -> out bf16 [T, d] (device), then the bias
  * update from this step's loads when update_bias != 0. Launch sequence:
- * route, permute (with FP8 quantisation of the rows when fp8), grouped GEMM 1
- * with SwiGLU, grouped GEMM 2, combine, bias update. */
+ * route, permute (with FP8 quantisation of the rows when fp8; it also counts
+ * the loads), grouped GEMM 1 with SwiGLU, grouped GEMM 2, combine, bias
+ * update. */
 moe_status moe_layer_forward(const moe_layer_weights* w, const uint16_t* u, int64_t T, uint16_t* out,
                              const moe_layer_outputs* outs, int update_bias,
                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
