@@ -22,8 +22,9 @@
 //                   H and dA, stored in bf16 and quantised per 1x128 tile
 //   kblock_offsets  each group's first 128-row block in the padded K layout
 //   pad_rows        the permuted row of every padded row of that layout
-//   quant_t         the weight-gradient operands: 128 rows x 64 columns per
-//                   block, transposed, one scale per (128 rows, column)
+//   quant_t         the weight-gradient operands: 128 rows x 512 columns per
+//                   block (a cp.async ring of 64-column chunks), transposed,
+//                   one scale per (128 rows, column)
 //   unpermute_bwd   one block per token: gate backward and du
 //   centroid_grad   de_i = sum over expert i's rows of dz u_t, in row order
 //   fp8_transpose   128x128 E4M3 blocks transposed with their scales
@@ -87,21 +88,39 @@ __global__ void __launch_bounds__(32 * (kMaxK + 1)) combine_bwd_kernel(
     const uint4* Gp = reinterpret_cast<const uint4*>(G + t * d);
     const uint4* yp = reinterpret_cast<const uint4*>(y + row * d);
     float acc = 0.0f;
-    for (int c = lane; c < d / 8; c += 32) {
-        float gv[8];
-        unpack8(__ldg(Gp + c), gv);
-        if (routed) {
-            float yv[8];
-            unpack8(__ldg(yp + c), yv);
+    // d % 256 == 0 (the layer's rule): every lane of the warp runs each step, as the
+    // shuffles of the tile's amax require. Two steps' loads are issued before either
+    // is used (bytes in flight for HBM); the dot product keeps its step order.
+    constexpr int kU = 2;
+    const int steps = d / 256;
+    for (int s0 = 0; s0 < steps; s0 += kU) {
+        uint4 gr[kU], yr[kU];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc = fmaf(gv[i], yv[i], acc);
+        for (int u = 0; u < kU; ++u) {
+            if (s0 + u < steps) {   // warp-uniform
+                const int c = lane + 32 * (s0 + u);
+                gr[u] = __ldg(Gp + c);
+                if (routed) yr[u] = __ldg(yp + c);
+            }
         }
-        uint2 codes;
-        // d % 256 == 0 (the layer's rule): every lane of the warp runs each step, as
-        // the shuffles of the tile's amax require
-        const float sc = quant8_tile16(gv, codes);
-        *reinterpret_cast<uint2*>(qdy + row * d + int64_t(c) * 8) = codes;
-        if ((lane & 15) == 0) sdy[(int64_t(c) / 16) * R + row] = routed ? __fmul_rn(g, sc) : sc;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (s0 + u < steps) {
+                const int c = lane + 32 * (s0 + u);
+                float gv[8];
+                unpack8(gr[u], gv);
+                if (routed) {
+                    float yv[8];
+                    unpack8(yr[u], yv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc = fmaf(gv[i], yv[i], acc);
+                }
+                uint2 codes;
+                const float sc = quant8_tile16(gv, codes);
+                *reinterpret_cast<uint2*>(qdy + row * d + int64_t(c) * 8) = codes;
+                if ((lane & 15) == 0) sdy[(int64_t(c) / 16) * R + row] = routed ? __fmul_rn(g, sc) : sc;
+            }
+        }
     }
     if (routed) {
         // a fixed xor tree over the warp's partial sums
@@ -222,21 +241,51 @@ struct QuantTArgs {
     float* s;                   // [Kp/128][C]
 };
 
-// One block per (128-row block b of the padded layout, 64 columns): rows of
-// the block gathered into shared memory as fp32, then per column the amax of
-// its 128 rows, the scale and the codes, written transposed. Row blocks are
-// adjacent in the grid, so the blocks running side by side write adjacent
-// 128-byte pieces of each output row (column blocks adjacent instead, to read
-// whole source rows together, measured 1.2x slower).
+// 16-byte cp.async that writes zeros, and reads nothing, when `bytes` is 0.
+__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kQtStages = 3;                // 64-column chunks in shared memory per block
+constexpr int kQtChunks = 8;                // chunks per block
+constexpr int kQtChunkBytes = 128 * 128;    // 128 rows x 64 bf16 columns
+
+template <int kSrc>
+__host__ __device__ constexpr int qt_sources() {   // SwiGLU: the gate and the up products
+    return kSrc == kSrcSwiglu ? 2 : 1;
+}
+template <int kSrc>
+__host__ __device__ constexpr int qt_smem_bytes() {
+    return kQtStages * qt_sources<kSrc>() * kQtChunkBytes;
+}
+
+// One block per (128-row block b of the padded layout, 8 chunks of 64
+// columns). The block looks its 128 source rows up once, then streams the
+// chunks through a 3-stage cp.async ring: while it quantises chunk j, chunks
+// j+1 and j+2 are in flight. Per chunk and column: the amax of the column's 128
+// rows, the scale and the codes, written transposed. Row blocks are adjacent in
+// the grid, so the blocks running side by side write adjacent 128-byte pieces
+// of each output row.
+// Shared layout of a chunk: row r's 128 bytes as eight 16-byte pieces, piece k
+// at place k ^ (r / 16 % 8). A thread of the quantisation reads one 32-bit
+// word (two columns) of 16 rows, 16 rows apart from its neighbours: with the
+// swizzle the 32 lanes of a warp hit 32 banks.
 template <int kSrc>
 __global__ void __launch_bounds__(256) quant_t_kernel(const QuantTArgs a) {
-    __shared__ float tile[128][65];
+    constexpr int kL = qt_sources<kSrc>();
+    extern __shared__ __align__(128) uint8_t qt_ring[];   // [kQtStages][kL][128 rows][128 bytes]
     __shared__ int row_src[128];
     __shared__ float row_w[128];
     const int64_t b = blockIdx.x;
-    const int c0 = blockIdx.y * 64;
     const int tid = threadIdx.x;
     if (b >= a.kofs[a.G]) return;   // block-uniform: K blocks past the last group are never read
+    const int j0 = int(blockIdx.y) * kQtChunks;
+    const int nj = min(kQtChunks, a.C / 64 - j0);
     if (tid < 128) {
         const int r = a.prow[b * 128 + tid];
         int srow = -1;
@@ -250,57 +299,95 @@ __global__ void __launch_bounds__(256) quant_t_kernel(const QuantTArgs a) {
         row_w[tid] = wgt;
     }
     __syncthreads();
-    // gather: 8 lanes per row (8 bf16 columns each), 32 rows per pass
-    {
-        const int rr = tid >> 3, cc = (tid & 7) * 8;
-        for (int i = rr; i < 128; i += 32) {
-            const int sr = row_src[i];
-            float f[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (sr >= 0) {
-                if (kSrc == kSrcSwiglu) {
-                    // output column c: gate product at 256 (c / 128) + c % 128, up product 128 further
-                    const int c = c0 + cc;
-                    const int64_t base = int64_t(sr) * (2 * a.C) + 256 * (c / 128) + (c % 128);
-                    float h1[8], h3[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(a.src + base)), h1);
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(a.src + base + 128)), h3);
+    const uint32_t ring = smem_u32(qt_ring);
+    // copies: a thread moves piece k of rows rr, rr + 32, rr + 64, rr + 96 (padding rows: zeros)
+    const int k = tid & 7, rr = tid >> 3;
+    auto issue = [&](int j) {
+        const uint32_t st = ring + uint32_t((j % kQtStages) * kL * kQtChunkBytes);
+        const int c = (j0 + j) * 64 + 8 * k;   // the piece's first column
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = h1[j] * sigmoid_f(h1[j]) * h3[j];
-                } else {
-                    unpack8(__ldg(reinterpret_cast<const uint4*>(a.src + int64_t(sr) * a.C + c0 + cc)), f);
-                    if (kSrc == kSrcScaledG) {
-                        const float wg = row_w[i];
+        for (int i = 0; i < 4; ++i) {
+            const int r = rr + 32 * i;
+            const int sr = row_src[r];
+            const int64_t srow = sr >= 0 ? sr : 0;
+            const uint32_t place = uint32_t(r) * 128u + uint32_t((k ^ ((r >> 4) & 7)) * 16);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) f[j] = wg * f[j];
-                    }
-                }
+            for (int l = 0; l < kL; ++l) {
+                // SwiGLU: output column c reads the gate product at 256 (c / 128) + c % 128
+                // and the up product 128 further
+                const uint16_t* src = kSrc == kSrcSwiglu
+                                          ? a.src + srow * (2 * a.C) + 256 * (c / 128) + (c % 128) + 128 * l
+                                          : a.src + srow * a.C + c;
+                cp_async_16z(st + uint32_t(l * kQtChunkBytes) + place, src, sr >= 0 ? 16u : 0u);
             }
+        }
+    };
 #pragma unroll
-            for (int j = 0; j < 8; ++j) tile[i][cc + j] = f[j];
+    for (int j = 0; j < kQtStages - 1; ++j) {
+        if (j < nj) issue(j);
+        cp_async_commit();
+    }
+    // quantisation: a thread takes columns 2 cp, 2 cp + 1 of rows 16 qt .. 16 qt + 15
+    const int qt = tid & 7, cp = tid >> 3;
+    for (int j = 0; j < nj; ++j) {
+        cp_async_wait_group<kQtStages - 2>();   // this thread's copies of chunk j have landed
+        __syncthreads();                        // ... and every thread's; chunk j - 1 is read
+        if (j + kQtStages - 1 < nj) issue(j + kQtStages - 1);
+        cp_async_commit();
+        const uint8_t* st = qt_ring + (j % kQtStages) * kL * kQtChunkBytes;
+        const int word = (((cp >> 2) ^ qt) * 16) + (cp & 3) * 4;   // rows 16 qt..: r / 16 % 8 = qt
+        float v0[16], v1[16];
+        float am0 = 0.0f, am1 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * qt + i;
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(st + r * 128 + word);
+            if (kSrc == kSrcSwiglu) {
+                const uint32_t w3 = *reinterpret_cast<const uint32_t*>(st + kQtChunkBytes + r * 128 + word);
+                const float g0 = bf16_lo(w), g1 = bf16_hi(w);
+                v0[i] = g0 * sigmoid_f(g0) * bf16_lo(w3);
+                v1[i] = g1 * sigmoid_f(g1) * bf16_hi(w3);
+            } else if (kSrc == kSrcScaledG) {
+                const float wg = row_w[r];
+                v0[i] = wg * bf16_lo(w);
+                v1[i] = wg * bf16_hi(w);
+            } else {
+                v0[i] = bf16_lo(w);
+                v1[i] = bf16_hi(w);
+            }
+            am0 = fmaxf(am0, fabsf(v0[i]));
+            am1 = fmaxf(am1, fabsf(v1[i]));
+        }
+        // the 8 lanes of a column pair: lane bits 0-2
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, o));
+            am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, o));
+        }
+        const float sc0 = tile_scale(am0), sc1 = tile_scale(am1);
+        // the quotients by reciprocal where that cannot change a code (e4m3_quotient): with
+        // IEEE divisions alone this kernel was bound by them (2.6 ms against 1.7 ms at the
+        // V3 training shape)
+        const float r0 = e4m3_recip(sc0), r1 = e4m3_recip(sc1);
+        uint32_t q0[4], q1[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            q0[m] = pack_e4m3x2(e4m3_quotient(v0[4 * m], sc0, r0), e4m3_quotient(v0[4 * m + 1], sc0, r0)) |
+                    (pack_e4m3x2(e4m3_quotient(v0[4 * m + 2], sc0, r0), e4m3_quotient(v0[4 * m + 3], sc0, r0))
+                     << 16);
+            q1[m] = pack_e4m3x2(e4m3_quotient(v1[4 * m], sc1, r1), e4m3_quotient(v1[4 * m + 1], sc1, r1)) |
+                    (pack_e4m3x2(e4m3_quotient(v1[4 * m + 2], sc1, r1), e4m3_quotient(v1[4 * m + 3], sc1, r1))
+                     << 16);
+        }
+        const int col = (j0 + j) * 64 + 2 * cp;
+        uint8_t* dst = a.q + int64_t(col) * a.Kp + b * 128 + 16 * qt;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(q0[0], q0[1], q0[2], q0[3]);
+        *reinterpret_cast<uint4*>(dst + a.Kp) = make_uint4(q1[0], q1[1], q1[2], q1[3]);
+        if (qt == 0) {
+            a.s[b * a.C + col] = sc0;
+            a.s[b * a.C + col + 1] = sc1;
         }
     }
-    __syncthreads();
-    // 4 lanes per column, 32 rows each
-    const int col = tid >> 2, qt = tid & 3;
-    float v[32];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        v[i] = tile[32 * qt + i][col];
-        amax = fmaxf(amax, fabsf(v[i]));
-    }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const float sc = tile_scale(amax);
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        w[i] = pack_e4m3x2(__fdiv_rn(v[4 * i], sc), __fdiv_rn(v[4 * i + 1], sc)) |
-               (pack_e4m3x2(__fdiv_rn(v[4 * i + 2], sc), __fdiv_rn(v[4 * i + 3], sc)) << 16);
-    uint4* dst = reinterpret_cast<uint4*>(a.q + int64_t(c0 + col) * a.Kp + b * 128 + 32 * qt);
-    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    if (qt == 0) a.s[b * a.C + c0 + col] = sc;
 }
 
 // One block of 256 threads per token: the gate backward (K scalars, thread 0)
@@ -561,16 +648,22 @@ cudaError_t launch_quant_t(int src_kind, const int32_t* prow, const int32_t* kof
                            const int32_t* perm_token, const float* row_gate, const uint16_t* src, int C,
                            int64_t Kp, uint8_t* q, float* s, cudaStream_t stream) {
     QuantTArgs a{prow, kofs, G, TK, perm_token, row_gate, src, C, Kp, q, s};
-    const dim3 grid(unsigned(Kp / 128), unsigned(C / 64));
-    if (grid.x == 0) return cudaSuccess;
+    const dim3 grid(unsigned(Kp / 128), unsigned((C / 64 + kQtChunks - 1) / kQtChunks));
+    if (grid.x == 0 || C == 0) return cudaSuccess;
+    cudaError_t e;
+    auto run = [&](auto kernel, int bytes, PerDeviceOnce& once) {
+        if ((e = allow_smem(once, kernel, bytes)) != cudaSuccess) return e;
+        kernel<<<grid, 256, bytes, stream>>>(a);
+        return cudaGetLastError();
+    };
+    static PerDeviceOnce o0, o1, o2, o3;
     switch (src_kind) {
-        case kSrcScaledG: quant_t_kernel<kSrcScaledG><<<grid, 256, 0, stream>>>(a); break;
-        case kSrcTokens: quant_t_kernel<kSrcTokens><<<grid, 256, 0, stream>>>(a); break;
-        case kSrcRows: quant_t_kernel<kSrcRows><<<grid, 256, 0, stream>>>(a); break;
-        case kSrcSwiglu: quant_t_kernel<kSrcSwiglu><<<grid, 256, 0, stream>>>(a); break;
+        case kSrcScaledG: return run(quant_t_kernel<kSrcScaledG>, qt_smem_bytes<kSrcScaledG>(), o0);
+        case kSrcTokens: return run(quant_t_kernel<kSrcTokens>, qt_smem_bytes<kSrcTokens>(), o1);
+        case kSrcRows: return run(quant_t_kernel<kSrcRows>, qt_smem_bytes<kSrcRows>(), o2);
+        case kSrcSwiglu: return run(quant_t_kernel<kSrcSwiglu>, qt_smem_bytes<kSrcSwiglu>(), o3);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_unpermute_bwd(const uint16_t* G, const uint16_t* dX, const int32_t* dest, const int32_t* topk,

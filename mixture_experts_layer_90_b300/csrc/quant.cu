@@ -2,7 +2,9 @@
 // Report, learn.ifs.name summary, paragraph on FP8 scaling): one fp32 scale per
 // 1x128 activation tile and per 128x128 weight block; scale = amax / 448
 // (1 for an all-zero tile) and q = e4m3(x / scale), both IEEE fp32 divisions,
-// conversion with round-to-nearest-even and saturation to +-448.
+// conversion with round-to-nearest-even and saturation to +-448. The 1x128
+// kernel forms x / scale by reciprocal where that gives the same code
+// (e4m3_quotient) and divides elsewhere.
 //
 // Both kernels stream bf16 in and e4m3 out with 16-byte loads; they are HBM
 // bound (3 bytes of traffic per element).
@@ -37,12 +39,12 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const uint16_t* __rest
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float sc = tile_scale(amax);
+        const float sc = tile_scale(amax), rc = e4m3_recip(sc);
         if (active) {
-            uint32_t w0 = pack_e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
-                          (pack_e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
-            uint32_t w1 = pack_e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
-                          (pack_e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
+            uint32_t w0 = pack_e4m3x2(e4m3_quotient(f[0], sc, rc), e4m3_quotient(f[1], sc, rc)) |
+                          (pack_e4m3x2(e4m3_quotient(f[2], sc, rc), e4m3_quotient(f[3], sc, rc)) << 16);
+            uint32_t w1 = pack_e4m3x2(e4m3_quotient(f[4], sc, rc), e4m3_quotient(f[5], sc, rc)) |
+                          (pack_e4m3x2(e4m3_quotient(f[6], sc, rc), e4m3_quotient(f[7], sc, rc)) << 16);
             reinterpret_cast<uint2*>(q + r * cols + kb * 128)[l] = make_uint2(w0, w1);
             if (l == 0) scales[kb * ld_s + r] = sc;
         }

@@ -96,6 +96,29 @@ def test_e4m3_conversion_every_bf16_value():
     np.testing.assert_array_equal(q.cpu().numpy(), oracle.e4m3_encode(v))
 
 
+def test_quant_1x128_every_bf16_value_under_many_scales():
+    """The quantiser forms x / scale by reciprocal where that cannot change the
+    code (and divides elsewhere): every bf16 value up to a tile's amax, for amax
+    in many binades (tiny ones whose scale is below the smallest normal float
+    included), must give the oracle's codes, which come from IEEE divisions."""
+    rng = np.random.Generator(np.random.PCG64(9))
+    amax_bits = np.concatenate([rng.integers(0x0080, 0x7F80, 24), [0x43E0, 0x3F80, 0x0200, 0x0480, 0x0500, 0x7F7F]])
+    rows = []
+    for ab in amax_bits.astype(np.uint32):
+        amax = np.array([ab << 16], np.uint32).view(np.float32)[0]
+        g = (np.arange(0, ab + 1, dtype=np.uint32) << 16).view(np.float32)
+        g = np.concatenate([g, -g])
+        g = np.concatenate([g, np.zeros((-g.size) % 127, np.float32)]).reshape(-1, 127)
+        rows.append(np.concatenate([np.full((g.shape[0], 1), amax, np.float32), g], axis=1))
+    v = np.concatenate(rows)
+    x = torch.from_numpy(v).to(torch.bfloat16)
+    q, s = lib().fp8_quant_1x128(cuda(x))
+    qo, so = oracle.quant_1x128(x)
+    np.testing.assert_array_equal(s.cpu().numpy(), so.T)
+    np.testing.assert_array_equal(q.cpu().numpy(), qo)
+    status_ok()
+
+
 # --------------------------------------------------------------------------
 # FP8 GEMMs
 # --------------------------------------------------------------------------
