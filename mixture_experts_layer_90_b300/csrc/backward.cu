@@ -32,6 +32,7 @@
 //                   128x128 quantisation, stored as is and transposed
 // All HBM bound; every sum runs in a fixed order (results reproducible bit for bit).
 #include "common.cuh"
+#include "e4m3.cuh"
 #include "kernels.cuh"
 
 namespace moe {

@@ -9,6 +9,7 @@
 // Both kernels stream bf16 in and e4m3 out with 16-byte loads; they are HBM
 // bound (3 bytes of traffic per element).
 #include "common.cuh"
+#include "e4m3.cuh"
 #include "kernels.cuh"
 
 namespace moe {
