@@ -18,8 +18,8 @@
 //   combine_bwd     one warp per (token, row): dg_{t,k} = G_t . y_{row(t,k)} and
 //                   the dgrad operand dY = g G_t per 1x128 tile (G_t's codes, g
 //                   times its scales)
-//   swiglu_bwd      one warp per (row, 128 outputs): dH from the stored bf16
-//                   H and dA, stored in bf16 and quantised per 1x128 tile
+//   swiglu_bwd      one half-warp per (row, 128 outputs): dH from the stored
+//                   bf16 H and dA, stored in bf16 and quantised per 1x128 tile
 //   kblock_offsets  each group's first 128-row block in the padded K layout
 //   pad_rows        the permuted row of every padded row of that layout
 //   quant_t         the weight-gradient operands: 128 rows x 512 columns per
@@ -136,49 +136,66 @@ __global__ void __launch_bounds__(32 * (kMaxK + 1)) combine_bwd_kernel(
     }
 }
 
-// One warp per (row r, pair p of 128-column blocks): lanes hold 4 of the 128
-// outputs. H's columns 256p.. are the gate products, 256p+128.. the up ones.
+// One half-warp per (row r, pair p of 128-column blocks): lanes hold 8 of the
+// 128 outputs (16-byte loads and stores). H's columns 256p.. are the gate
+// products, 256p+128.. the up ones. The two halves of a warp take consecutive
+// items; a half past the last item computes on zeros and stores nothing (the
+// amax shuffles stay inside a half).
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t* __restrict__ dA,
                                                          const uint16_t* __restrict__ H, int64_t R, int I,
                                                          uint16_t* __restrict__ dH, uint8_t* __restrict__ qdh,
                                                          float* __restrict__ sdh) {
-    const int lane = threadIdx.x & 31;
+    const int hl = threadIdx.x & 15;
     const int pairs = I / 128;
-    const int64_t item = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (item >= R * pairs) return;   // warp-uniform
-    const int64_t r = item / pairs;
-    const int p = int(item - r * pairs);
+    const int64_t item = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 4;
+    const bool active = item < R * pairs;
+    const int64_t r = active ? item / pairs : 0;
+    const int p = active ? int(item - r * pairs) : 0;
     const int I2 = 2 * I;
-    const uint2 va = __ldg(reinterpret_cast<const uint2*>(dA + r * I + 128 * p) + lane);
-    const uint2 v1 = __ldg(reinterpret_cast<const uint2*>(H + r * I2 + 256 * p) + lane);
-    const uint2 v3 = __ldg(reinterpret_cast<const uint2*>(H + r * I2 + 256 * p + 128) + lane);
-    const float a[4] = {bf16_lo(va.x), bf16_hi(va.x), bf16_lo(va.y), bf16_hi(va.y)};
-    const float h1[4] = {bf16_lo(v1.x), bf16_hi(v1.x), bf16_lo(v1.y), bf16_hi(v1.y)};
-    const float h3[4] = {bf16_lo(v3.x), bf16_hi(v3.x), bf16_lo(v3.y), bf16_hi(v3.y)};
-    float d1[4], d3[4];
+    uint4 va = make_uint4(0u, 0u, 0u, 0u), v1 = va, v3 = va;
+    if (active) {
+        va = __ldg(reinterpret_cast<const uint4*>(dA + r * I + 128 * p) + hl);
+        v1 = __ldg(reinterpret_cast<const uint4*>(H + r * I2 + 256 * p) + hl);
+        v3 = __ldg(reinterpret_cast<const uint4*>(H + r * I2 + 256 * p + 128) + hl);
+    }
+    float a[8], h1[8], h3[8];
+    unpack8(va, a);
+    unpack8(v1, h1);
+    unpack8(v3, h3);
+    float d1[8], d3[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const float sg = sigmoid_f(h1[i]);
         d1[i] = a[i] * h3[i] * sg * (1.0f + h1[i] * (1.0f - sg));
         d3[i] = a[i] * h1[i] * sg;
     }
     // stored in bf16; the quantisation below reads the stored values
-    const uint2 b1 = make_uint2(pack_bf16x2(d1[0], d1[1]), pack_bf16x2(d1[2], d1[3]));
-    const uint2 b3 = make_uint2(pack_bf16x2(d3[0], d3[1]), pack_bf16x2(d3[2], d3[3]));
-    reinterpret_cast<uint2*>(dH + r * I2 + 256 * p)[lane] = b1;
-    reinterpret_cast<uint2*>(dH + r * I2 + 256 * p + 128)[lane] = b3;
+    const uint4 b1 = make_uint4(pack_bf16x2(d1[0], d1[1]), pack_bf16x2(d1[2], d1[3]), pack_bf16x2(d1[4], d1[5]),
+                                pack_bf16x2(d1[6], d1[7]));
+    const uint4 b3 = make_uint4(pack_bf16x2(d3[0], d3[1]), pack_bf16x2(d3[2], d3[3]), pack_bf16x2(d3[4], d3[5]),
+                                pack_bf16x2(d3[6], d3[7]));
+    if (active) {
+        reinterpret_cast<uint4*>(dH + r * I2 + 256 * p)[hl] = b1;
+        reinterpret_cast<uint4*>(dH + r * I2 + 256 * p + 128)[hl] = b3;
+    }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-        const uint2 b = half ? b3 : b1;
-        const float f[4] = {bf16_lo(b.x), bf16_hi(b.x), bf16_lo(b.y), bf16_hi(b.y)};
-        float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
+        float f[8];
+        unpack8(half ? b3 : b1, f);
+        float amax = 0.0f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float sc = tile_scale(amax);
-        const uint32_t q = pack_e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
-                           (pack_e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
-        reinterpret_cast<uint32_t*>(qdh + r * I2 + 256 * p + 128 * half)[lane] = q;
-        if (lane == 0) sdh[int64_t(2 * p + half) * R + r] = sc;
+        const uint2 q = make_uint2(pack_e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
+                                       (pack_e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16),
+                                   pack_e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
+                                       (pack_e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16));
+        if (active) {
+            reinterpret_cast<uint2*>(qdh + r * I2 + 256 * p + 128 * half)[hl] = q;
+            if (hl == 0) sdh[int64_t(2 * p + half) * R + r] = sc;
+        }
     }
 }
 
@@ -627,9 +644,9 @@ cudaError_t launch_combine_bwd(const uint16_t* G, const uint16_t* y, const float
 
 cudaError_t launch_swiglu_bwd(const uint16_t* dA, const uint16_t* H, int64_t R, int I, uint16_t* dH, uint8_t* qdh,
                               float* sdh, cudaStream_t stream) {
-    const int64_t warps = R * (I / 128);
-    if (warps == 0) return cudaSuccess;
-    swiglu_bwd_kernel<<<unsigned((warps + 7) / 8), 256, 0, stream>>>(dA, H, R, I, dH, qdh, sdh);
+    const int64_t items = R * (I / 128);   // a half-warp each, 16 per block
+    if (items == 0) return cudaSuccess;
+    swiglu_bwd_kernel<<<unsigned((items + 15) / 16), 256, 0, stream>>>(dA, H, R, I, dH, qdh, sdh);
     return cudaGetLastError();
 }
 
