@@ -77,10 +77,97 @@ def peaks():
     return FALLBACK, "fallback"
 
 
+class NvmlPoller:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, by ctypes; read-only queries) every ~2 ms in a thread, so
+    that a timed region of a tenth of a second still gets dozens of samples.
+    Inactive when the library cannot be loaded."""
+
+    # nvmlClocksEventReason* bits
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4))
+    CLOCK_SM = 1
+
+    def __init__(self, gpu_index: int):
+        self.samples = []          # (sm_mhz, reason bits)
+        self.on = False
+        self.lib = None
+        try:
+            import ctypes
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self._index(lib, gpu_index)),
+                                                 ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(mx)) != 0:
+                return
+            self.max_mhz = float(mx.value)
+            self.get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ctypes = ctypes
+            self.lib = lib
+        except (OSError, AttributeError):
+            self.lib = None
+
+    @staticmethod
+    def _index(lib, gpu_index):
+        # the NVML device with the CUDA device's UUID, else the same index
+        try:
+            import ctypes
+            import torch
+            want = str(torch.cuda.get_device_properties(gpu_index).uuid)
+            n = ctypes.c_uint()
+            lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+            for i in range(n.value):
+                h = ctypes.c_void_p()
+                buf = ctypes.create_string_buffer(96)
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(i), ctypes.byref(h)) == 0 and \
+                        lib.nvmlDeviceGetUUID(h, buf, ctypes.c_uint(96)) == 0 and want and want in buf.value.decode():
+                    return i
+        except Exception:
+            pass
+        return gpu_index
+
+    def start(self):
+        if self.lib is None:
+            return
+        self.on = True
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        if self.on:
+            self.on = False
+            self._t.join(timeout=2.0)
+
+    def _run(self):
+        ct = self.ctypes
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while self.on:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(clk)) != 0 or \
+                    self.get_reasons(self.h, ct.byref(rs)) != 0:
+                return
+            self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.002)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        sm = [c for c, _ in self.samples]
+        reasons = sorted(name for name, bit in self.REASONS if any(r & bit for _, r in self.samples))
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sm), "source": "NVML, every ~2 ms"}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 20 ms; summary()
-    covers the samples taken between mark_start() and mark_stop() (the timed
-    region), or all samples if no mark was set."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms, plus NVML
+    polled every ~2 ms (NvmlPoller); summary() covers the samples taken between
+    mark_start() and mark_stop() (the timed region), or all samples if no mark
+    was set. The NVML samples are the record when there are any; the
+    nvidia-smi summary is kept beside them."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -91,6 +178,7 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.start, self.stop = 0, None
+        self.nvml = NvmlPoller(gpu_index)
 
     def __enter__(self):
         try:
@@ -108,8 +196,10 @@ class ClockSampler:
 
     def mark_start(self):
         self.start = len(self.lines)
+        self.nvml.start()
 
     def mark_stop(self):
+        self.nvml.stop()
         time.sleep(0.05)          # let the sampler report the region's last interval
         self.stop = len(self.lines)
 
@@ -118,6 +208,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.nvml.stop()
         if self.stop is None:
             self.stop = len(self.lines)
         if self.proc:
@@ -142,8 +233,15 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        smi = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+               "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, every 20 ms"}
+        fine = self.nvml.summary()
+        if fine is None:
+            return smi
+        # a reason either source saw during the region counts
+        fine["reasons"] = sorted(set(fine["reasons"]) | set(smi["reasons"]))
+        fine["nvidia_smi"] = smi
+        return fine
 
 
 def max_over_ranks(x: float, device) -> float:

@@ -75,12 +75,16 @@ constexpr int kMaxK = 16;
 // is a half-warp, and a warp steps over d 256 columns at a time.
 // The dgrad operand of a routed row is the tile rule applied to g G_t: the
 // rule is scale-invariant (amax and every value scale by g), so its codes are
-// those of G_t's tile and its scale is g times G_t's. Every warp quantises
-// G_t's tiles itself (the same codes) and writes them to its row.
+// those of G_t's tile and its scale is g times G_t's. The block quantises G_t
+// once (its warps share the steps) into shared memory, and every warp copies
+// the codes to its row.
 __global__ void __launch_bounds__(32 * (kMaxK + 1)) combine_bwd_kernel(
     const uint16_t* __restrict__ G, const uint16_t* __restrict__ y, const float* __restrict__ gates,
     const int32_t* __restrict__ dest, int64_t T, int d, int K, int64_t R, uint8_t* __restrict__ qdy,
     float* __restrict__ sdy, float* __restrict__ row_gate, float* __restrict__ dg) {
+    extern __shared__ __align__(16) uint8_t cb_smem[];
+    uint2* codes_sm = reinterpret_cast<uint2*>(cb_smem);               // [d / 8]: G_t's codes
+    float* scale_sm = reinterpret_cast<float*>(cb_smem + d);           // [d / 128]: its tile scales
     const int64_t t = blockIdx.x;
     const int lane = threadIdx.x & 31, k = threadIdx.x >> 5;
     const bool routed = k < K;
@@ -88,38 +92,51 @@ __global__ void __launch_bounds__(32 * (kMaxK + 1)) combine_bwd_kernel(
     const float g = routed ? __ldg(gates + t * K + k) : 1.0f;
     const uint4* Gp = reinterpret_cast<const uint4*>(G + t * d);
     const uint4* yp = reinterpret_cast<const uint4*>(y + row * d);
-    float acc = 0.0f;
-    // d % 256 == 0 (the layer's rule): every lane of the warp runs each step, as the
-    // shuffles of the tile's amax require. Two steps' loads are issued before either
-    // is used (bytes in flight for HBM); the dot product keeps its step order.
-    constexpr int kU = 2;
+    // d % 256 == 0 (the layer's rule): every lane of a warp runs each step, as the
+    // shuffles of the tile's amax require
     const int steps = d / 256;
+    for (int st = k; st < steps; st += K + 1) {   // warp-uniform
+        const int c = lane + 32 * st;
+        float gv[8];
+        unpack8(__ldg(Gp + c), gv);
+        uint2 codes;
+        const float sc = quant8_tile16(gv, codes);
+        codes_sm[c] = codes;
+        if ((lane & 15) == 0) scale_sm[c / 16] = sc;
+    }
+    __syncthreads();
+    float acc = 0.0f;
+    // Two steps' loads are issued before either is used (bytes in flight for HBM);
+    // the dot product keeps its step order.
+    constexpr int kU = 2;
     for (int s0 = 0; s0 < steps; s0 += kU) {
         uint4 gr[kU], yr[kU];
+        if (routed) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            if (s0 + u < steps) {   // warp-uniform
-                const int c = lane + 32 * (s0 + u);
-                gr[u] = __ldg(Gp + c);
-                if (routed) yr[u] = __ldg(yp + c);
+            for (int u = 0; u < kU; ++u) {
+                if (s0 + u < steps) {
+                    const int c = lane + 32 * (s0 + u);
+                    gr[u] = __ldg(Gp + c);
+                    yr[u] = __ldg(yp + c);
+                }
             }
         }
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             if (s0 + u < steps) {
                 const int c = lane + 32 * (s0 + u);
-                float gv[8];
-                unpack8(gr[u], gv);
                 if (routed) {
-                    float yv[8];
+                    float gv[8], yv[8];
+                    unpack8(gr[u], gv);
                     unpack8(yr[u], yv);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) acc = fmaf(gv[i], yv[i], acc);
                 }
-                uint2 codes;
-                const float sc = quant8_tile16(gv, codes);
-                *reinterpret_cast<uint2*>(qdy + row * d + int64_t(c) * 8) = codes;
-                if ((lane & 15) == 0) sdy[(int64_t(c) / 16) * R + row] = routed ? __fmul_rn(g, sc) : sc;
+                *reinterpret_cast<uint2*>(qdy + row * d + int64_t(c) * 8) = codes_sm[c];
+                if ((lane & 15) == 0) {
+                    const float sc = scale_sm[c / 16];
+                    sdy[(int64_t(c) / 16) * R + row] = routed ? __fmul_rn(g, sc) : sc;
+                }
             }
         }
     }
@@ -637,8 +654,12 @@ cudaError_t launch_combine_bwd(const uint16_t* G, const uint16_t* y, const float
                                int64_t T, int d, int K, int64_t R, uint8_t* qdy, float* sdy, float* row_gate,
                                float* dg, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    combine_bwd_kernel<<<unsigned(T), 32 * (K + 1), 0, stream>>>(G, y, gates, dest, T, d, K, R, qdy, sdy, row_gate,
-                                                                 dg);
+    const int smem = d + d / 32;   // G_t's codes and tile scales
+    static PerDeviceOnce once;
+    cudaError_t e = allow_smem(once, combine_bwd_kernel, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    combine_bwd_kernel<<<unsigned(T), 32 * (K + 1), smem, stream>>>(G, y, gates, dest, T, d, K, R, qdy, sdy,
+                                                                    row_gate, dg);
     return cudaGetLastError();
 }
 
