@@ -924,6 +924,38 @@ def case_wgrad_slice(moe, S, dev, args, flush):
             "l2": "flushed before each launch"}
 
 
+def case_dispatch_modes(moe, S, dev, args):
+    """The V3 layer step under both dispatch modes of an FP8 layer, alternating in
+    one process on the same weights and batches: the permutation writing the
+    grouped rows (scatter, the default) and GEMM 1 gathering the quantised
+    tokens by perm_token (gather). Stages by CUDA events, ms per step."""
+    import torch
+    sh = S.LAYER_V3
+    layer = moe.MoELayer.build(sh.d, sh.N, sh.K, sh.I, S.centroids(sh, zipf=True).to(dev), S.bias(sh).to(dev),
+                               lambda e: S.expert_weights(sh, e, device=dev), fp8=True, gamma=sh.gamma)
+    u_bufs = [S.tokens(sh, seed=s, device=dev) for s in (0, 7)]
+    out = torch.empty_like(u_bufs[0])
+    n_ev = len(moe.LAYER_STAGES) + 1
+    runs = {"scatter": [], "gather": []}
+    for _ in range(2):
+        for name, mode in (("scatter", moe.MOE_DISPATCH_SCATTER), ("gather", moe.MOE_DISPATCH_GATHER)):
+            layer._desc.dispatch = mode
+            for i in range(args.warmup):
+                layer.forward(u_bufs[i % 2], out, update_bias=False)
+            torch.cuda.synchronize()
+            events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+            for i in range(args.steps):
+                layer.forward(u_bufs[i % 2], out, update_bias=False, stage_events=events[i])
+            torch.cuda.synchronize()
+            runs[name].append({n: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in events)
+                               for j, n in enumerate(moe.LAYER_STAGES)})
+    res = {"workload": "v3-layer-fp8 dispatch modes", "l2": "inputs larger than L2 (streamed weights)"}
+    for name, rs in runs.items():
+        stages = {n: statistics.mean(r[n] for r in rs) for n in moe.LAYER_STAGES}
+        res[name] = {"ms_per_step": sum(stages.values()), "stages_ms": stages}
+    return res
+
+
 def run_case(args):
     import torch
 
@@ -948,6 +980,8 @@ def run_case(args):
         line.update(case_train(moe, S, dev, args, flush, cpu_baseline=cb))
     elif args.case == "wgrad-small":
         line.update(case_wgrad_slice(moe, S, dev, args, flush))
+    elif args.case == "dispatch":
+        line.update(case_dispatch_modes(moe, S, dev, args))
     elif args.case in ("decode64", "decode256"):
         sh = S.LAYER_V3
         cent = S.centroids(sh, zipf=True).to(dev)
@@ -970,7 +1004,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="time the V3 layer only")
     ap.add_argument("--case", default="layer",
                     choices=["layer", "tiny", "route", "gemm", "gemm1-small", "gemm2-small", "decode64",
-                             "decode256", "permute-fp8", "combine", "train", "wgrad-small"],
+                             "decode256", "permute-fp8", "combine", "train", "wgrad-small", "dispatch"],
                     help="layer: the V3 layer step with every other workload (the benchmark line); the others "
                          "time one workload alone")
     args = ap.parse_args()

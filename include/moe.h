@@ -281,7 +281,20 @@ typedef struct {
     const float* w2_scales;    /* [N+1][d/128][I/128] (fp8 only)                            */
     const void* centroids_prepared; /* NULL, or the output of moe_route_prepare_centroids for
                                        `centroids` (then the layer routes from it)           */
+    int dispatch;              /* FP8 layers: MOE_DISPATCH_SCATTER (0) or MOE_DISPATCH_GATHER   */
 } moe_layer_weights;
+
+/* How an FP8 layer hands the tokens to grouped GEMM 1 (the dispatch):
+ *   MOE_DISPATCH_SCATTER  moe_permute writes every (token, k) row, quantised, to
+ *                         its place in the expert-grouped rows; GEMM 1 reads
+ *                         those rows by TMA.
+ *   MOE_DISPATCH_GATHER   the tokens are quantised once (fp8_quant_1x128), the
+ *                         permutation moves no rows, and GEMM 1 gathers each
+ *                         row of its A operand from the quantised tokens by
+ *                         perm_token (cp.async): the grouped rows are never
+ *                         written. The results are the same bits.
+ * bf16 layers always scatter. */
+enum { MOE_DISPATCH_SCATTER = 0, MOE_DISPATCH_GATHER = 1 };
 
 /* Optional outputs of one forward (any may be NULL except loads). */
 typedef struct {

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(HERE, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_WORKSPACE, \
     MOE_ERR_DEVICE_DATA = range(7)
 MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_DTYPE_E4M3 = 0, 1, 2
+MOE_DISPATCH_SCATTER, MOE_DISPATCH_GATHER = 0, 1
 MOE_EPI_BF16, MOE_EPI_SWIGLU_FP8, MOE_EPI_SWIGLU_BF16, MOE_EPI_F32 = 0, 1, 2, 3
 
 EXPORTS = [
@@ -54,6 +55,7 @@ class LayerWeights(ctypes.Structure):
         ("fp8", ctypes.c_int), ("centroids", ctypes.c_void_p), ("centroid_dtype", ctypes.c_int),
         ("bias", ctypes.c_void_p), ("w13", ctypes.c_void_p), ("w13_scales", ctypes.c_void_p),
         ("w2", ctypes.c_void_p), ("w2_scales", ctypes.c_void_p), ("centroids_prepared", ctypes.c_void_p),
+        ("dispatch", ctypes.c_int),
     ]
 
 

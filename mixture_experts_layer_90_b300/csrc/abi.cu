@@ -262,10 +262,13 @@ moe_status moe_permute(const uint16_t* x, int64_t T, int d, const int32_t* topk_
 }
 
 // fp8_grouped_gemm; with h_out (MOE_EPI_SWIGLU_FP8 only) the products are also
-// stored in bf16 [M_total, Nd] (the training forward keeps them).
+// stored in bf16 [M_total, Nd] (the training forward keeps them). With a_gather,
+// A is [a_rows][Kd] and the grouped A's row r is its row a_gather[r] (r < tk) or
+// r - tk; sa is [Kd/128][a_rows].
 static moe_status fp8_gemm_impl(const uint8_t* A, const float* sa, const uint8_t* B, const float* sb,
                                 const int32_t* group_offsets, int G, int64_t M_total, int Nd, int Kd, int epilogue,
-                                void* C, float* c_scales, uint16_t* h_out, moe_stream_t stream) {
+                                void* C, float* c_scales, uint16_t* h_out, moe_stream_t stream,
+                                const int32_t* a_gather = nullptr, int64_t tk = 0, int64_t a_rows = 0) {
     REQUIRE(G >= 1 && G <= moe::gemm_max_groups(), "fp8_grouped_gemm: G=%d must be in [1, 1024]", G);
     REQUIRE(M_total >= 0 && M_total <= kMaxRows, "fp8_grouped_gemm: M_total out of range");
     REQUIRE(Kd > 0 && Kd % 128 == 0, "fp8_grouped_gemm: Kd=%d must be a multiple of 128", Kd);
@@ -278,8 +281,9 @@ static moe_status fp8_gemm_impl(const uint8_t* A, const float* sa, const uint8_t
     REQUIRE(A && sa && C, "fp8_grouped_gemm: null pointer");
     REQUIRE(epilogue != MOE_EPI_SWIGLU_FP8 || c_scales, "fp8_grouped_gemm: SwiGLU output needs scales");
     REQUIRE(al16(A) && al32(C), "fp8_grouped_gemm: A must be 16-byte and C 32-byte aligned");
+    REQUIRE(!a_gather || (a_rows > 0 && tk >= 0 && tk <= M_total), "fp8_grouped_gemm: bad row gather");
     CUtensorMap ta, tb;
-    if (!moe::make_kmajor_map(&ta, A, false, uint64_t(Kd), uint64_t(M_total), uint64_t(Kd), 128) ||
+    if (!moe::make_kmajor_map(&ta, A, false, uint64_t(Kd), uint64_t(a_gather ? a_rows : M_total), uint64_t(Kd), 128) ||
         !moe::make_kmajor_map(&tb, B, false, uint64_t(Kd), uint64_t(G) * Nd, uint64_t(Kd), 256))
         return fail(MOE_ERR_CUDA, "fp8_grouped_gemm: tensor map encoding failed");
     moe::GemmArgs a{};
@@ -294,11 +298,14 @@ static moe_status fp8_gemm_impl(const uint8_t* A, const float* sa, const uint8_t
     a.splits = 1;
     a.epilogue = epilogue;
     a.sa = sa;
-    a.lda_s = M_total;
+    a.lda_s = a_gather ? a_rows : M_total;
     a.sb = sb;
     a.C = C;
     a.c_scales = c_scales;
     a.h_out = h_out;
+    a.a_gather = a_gather;
+    a.a_gather_tk = tk;
+    a.a_src = A;
     REQUIRE(!h_out || (epilogue == MOE_EPI_SWIGLU_FP8 && al32(h_out)), "fp8_grouped_gemm: bad product output");
     CUDA_OK(moe::run_grouped_gemm(moe::kModeFP8, ta, tb, a, moe::num_sms(), stream));
     return MOE_OK;
@@ -422,6 +429,8 @@ moe_status check_layer(const moe_layer_weights* w) {
     REQUIRE(w->N + 1 <= moe::gemm_max_groups(), "moe_layer: too many experts");
     REQUIRE(w->w13 && w->w2 && w->centroids && w->bias, "moe_layer: null weight pointer");
     REQUIRE(!w->fp8 || (w->w13_scales && w->w2_scales), "moe_layer: FP8 weights need scales");
+    REQUIRE(w->dispatch == MOE_DISPATCH_SCATTER || w->dispatch == MOE_DISPATCH_GATHER,
+            "moe_layer: dispatch=%d", w->dispatch);
     return MOE_OK;
 }
 
@@ -468,15 +477,26 @@ static moe_status layer_forward(const moe_layer_weights* w, const uint16_t* u, i
         STATUS_OK(route_impl(u, T, d, w->centroids, w->centroid_dtype, w->bias, N, K, w->n_groups, w->topk_groups,
                              topk, gates, nullptr, scores, ws + L.route, L.perm - L.route, stream, logits));
     STATUS_OK(mark(1));
-    STATUS_OK(permute_impl(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
-                           reinterpret_cast<int32_t*>(ws + L.perm_token), dest, ws + L.x_perm,
-                           reinterpret_cast<float*>(ws + L.x_scales), ws + L.perm, L.offsets - L.perm, stream, loads));
+    int32_t* perm_token = reinterpret_cast<int32_t*>(ws + L.perm_token);
+    const bool gather = w->fp8 && w->dispatch == MOE_DISPATCH_GATHER;
+    if (gather) {
+        // fused dispatch: the tokens quantised once into x_perm's space ([T][d] codes,
+        // [d/128][T] scales), the permutation without moving rows; GEMM 1 gathers them
+        CUDA_OK(moe::launch_quant_1x128(u, T, d, d, ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales), T,
+                                        stream));
+        CUDA_OK(moe::launch_permute(u, T, d, topk, N, K, MOE_DTYPE_E4M3, 1, offsets, perm_token, dest, nullptr,
+                                    nullptr, ws + L.perm, stream, loads));
+    } else {
+        STATUS_OK(permute_impl(u, T, d, topk, N, K, w->fp8 ? MOE_DTYPE_E4M3 : MOE_DTYPE_BF16, 1, offsets,
+                               perm_token, dest, ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales), ws + L.perm,
+                               L.offsets - L.perm, stream, loads));
+    }
     STATUS_OK(mark(2));
     if (w->fp8) {
         STATUS_OK(fp8_gemm_impl(ws + L.x_perm, reinterpret_cast<float*>(ws + L.x_scales),
                                 reinterpret_cast<const uint8_t*>(w->w13), w->w13_scales, offsets, N + 1, R, 2 * I, d,
                                 MOE_EPI_SWIGLU_FP8, ws + L.act, reinterpret_cast<float*>(ws + L.act_scales), h_out,
-                                stream));
+                                stream, gather ? perm_token : nullptr, T * K, T));
         STATUS_OK(mark(3));
         STATUS_OK(fp8_grouped_gemm(ws + L.act, reinterpret_cast<float*>(ws + L.act_scales),
                                    reinterpret_cast<const uint8_t*>(w->w2), w->w2_scales, offsets, N + 1, R, d, I,

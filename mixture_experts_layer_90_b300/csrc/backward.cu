@@ -276,16 +276,6 @@ struct QuantTArgs {
     float* s;                   // [Kp/128][C]
 };
 
-// 16-byte cp.async that writes zeros, and reads nothing, when `bytes` is 0.
-__device__ __forceinline__ void cp_async_16z(uint32_t dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 constexpr int kQtStages = 3;                // 64-column chunks in shared memory per block
 constexpr int kQtChunks = 8;                // chunks per block
 constexpr int kQtChunkBytes = 128 * 128;    // 128 rows x 64 bf16 columns

@@ -132,7 +132,7 @@ __device__ __forceinline__ void st_global_32B(void* p, const uint32_t* w) {   //
                  : "memory");
 }
 
-template <int kMode, int kEpi>
+template <int kMode, int kEpi, bool kGather = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
@@ -156,8 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------- prologue ----------------
     if (threadIdx.x == 0) {
+        // a gathered A arrives by cp.async: its stage gets a second arrival on full[]
+        const uint32_t full_count = kGather ? 2u : 1u;
         for (int i = 0; i < kSt; ++i) {
-            mbar_init(smem_u32(&s.full[i]), 1);
+            mbar_init(smem_u32(&s.full[i]), full_count);
             mbar_init(smem_u32(&s.empty[i]), 1);
         }
         for (int i = 0; i < kSSlots; ++i) {
@@ -229,7 +231,93 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = s.tmem_base;
     const int total = s.total_items;
 
-    if (warp == kProducerWarp) {
+    if (kGather && warp == kProducerWarp) {
+        // ---------------- A rows gathered by cp.async (every lane), B by TMA (lane 0) ----------------
+        // Row m of a tile is row a_gather[r] (routed rows r) or r - a_gather_tk (the shared
+        // expert's) of a_src; rows past the group's end read zeros (computed, never stored).
+        // Lane l copies rows l, l+32, l+64, l+96, all eight 16-byte pieces of each, into the
+        // layout the MMA descriptor reads: piece c of row m at c ^ (m % 8) (the 128-byte
+        // swizzle TMA would write). A stage gets its second arrival once this lane's copies
+        // into it have landed and a proxy fence has made them visible to the tensor core;
+        // copies run kAhead stages ahead of those arrivals. Measured at the V3 shape this
+        // feeds GEMM 1 at well under the TMA path's rate (4.8 against 2.8 ms): the one warp's
+        // copies and their completion waits, not the MMA, set the pace. Variants that were
+        // slower still: kAhead = 3 (the MMA then waits on every stage's arrival), and copies
+        // of four whole rows per warp instruction through a shared row table.
+        constexpr int kAhead = 2;
+        int stage = 0, sig = 0, pending = 0;
+        uint32_t phase = 0;
+        int armed[kStages] = {0, 0, 0, 0};
+        bool stop = false;
+        auto signal_oldest = [&]() {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.full[sig]));
+            if (++sig == kSt) sig = 0;
+            --pending;
+        };
+        for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
+            const Item it = decode(item, s, G, n_tiles_n, splits);
+            const int a_row = s.offs[it.g] + it.mt * kBM;
+            const int rows = s.offs[it.g + 1] - a_row;
+            const int b_row = it.g * args.Nd + it.nt * kBN;
+            const uint8_t* src[4];
+            uint32_t nbytes[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = lane + 32 * i;
+                src[i] = args.a_src;
+                nbytes[i] = 0u;
+                if (m < rows) {
+                    const int64_t r = int64_t(a_row) + m;
+                    const int64_t tok = r < args.a_gather_tk ? int64_t(__ldg(args.a_gather + r)) : r - args.a_gather_tk;
+                    src[i] = args.a_src + tok * int64_t(args.Kd);
+                    nbytes[i] = 16u;
+                }
+            }
+            const int k0 = it.sp * steps_per_split;
+            const int k1 = min(args.k_steps, k0 + steps_per_split);
+            for (int ks = k0; ks < k1; ++ks) {
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, abort);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t fb = smem_u32(&s.full[stage]);
+                    mbar_arrive_expect_tx(fb, kBBytes);
+                    tma_load_2d(ringB + stage * kBBytes, &tmB, fb, ks * args.elems_per_step, b_row);
+                    armed[stage] += 1;
+                }
+                const uint32_t dst = ringA + stage * kABytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = lane + 32 * i;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        cp_async_16z(dst + uint32_t(m * 128 + ((c ^ (m & 7)) * 16)), src[i] + ks * 128 + c * 16,
+                                     nbytes[i]);
+                }
+                cp_async_commit();
+                if (++pending > kAhead) {
+                    cp_async_wait_group<kAhead>();   // the oldest pending stage's copies have landed
+                    signal_oldest();
+                }
+                if (++stage == kSt) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        cp_async_wait_all();   // no copy into shared memory may outlive the block
+        while (pending > 0) signal_oldest();
+        // never leave the block while a TMA copy into its shared memory is in flight
+        if (lane == 0)
+            for (int i = 0; i < kSt; ++i)
+                if (armed[i] > 0) mbar_wait_limit(smem_u32(&s.full[i]), uint32_t(armed[i] - 1) & 1u, 200000000ull);
+        __syncwarp();
+    } else if (warp == kProducerWarp) {
         // ---------------- TMA producer: one lane, nothing else in its loop ----------------
         if (lane == 0) {
             int stage = 0;
@@ -311,11 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
                 const Item it = decode(item, s, G, n_tiles_n, splits);
                 const int a_row = s.offs[it.g] + it.mt * kBM;
-                // rows past a group's end are clamped into the matrix: computed, never stored
+                // rows past a group's end are clamped into the matrix: computed, never stored;
+                // a gathered A takes its rows' scales from the same source rows
                 const float* sa_src[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int64_t r = min(int64_t(a_row) + 4 * lane + i, args.M_total - 1);
+                    int64_t r = min(int64_t(a_row) + 4 * lane + i, args.M_total - 1);
+                    if (kGather)
+                        r = r < args.a_gather_tk ? int64_t(__ldg(args.a_gather + r)) : r - args.a_gather_tk;
                     sa_src[i] = args.sa + r;
                 }
                 const float* sb_src = args.sb + (int64_t(it.g) * (args.Nd / 128) + 2 * it.nt) * nkb;
@@ -758,14 +849,14 @@ bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inne
     return r == CUDA_SUCCESS;
 }
 
-template <int kMode, int kEpi>
+template <int kMode, int kEpi, bool kGather = false>
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
                           int grid, cudaStream_t stream) {
     static PerDeviceOnce once;
     constexpr size_t kSmemBytes = smem_bytes<kMode>();
-    cudaError_t e = allow_smem(once, grouped_gemm_kernel<kMode, kEpi>, int(kSmemBytes));
+    cudaError_t e = allow_smem(once, grouped_gemm_kernel<kMode, kEpi, kGather>, int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<kMode, kEpi><<<grid, kThreads, kSmemBytes, stream>>>(a, b, c, args);
+    grouped_gemm_kernel<kMode, kEpi, kGather><<<grid, kThreads, kSmemBytes, stream>>>(a, b, c, args);
     return cudaGetLastError();
 }
 
@@ -778,8 +869,11 @@ cudaError_t run_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& 
     }
     if (mode == kModeFP8) {
         if (args.epilogue == MOE_EPI_SWIGLU_FP8)
-            return launch<kModeFP8, MOE_EPI_SWIGLU_FP8>(a, b, cm, args, grid, stream);
-        if (args.epilogue == MOE_EPI_BF16) return launch<kModeFP8, MOE_EPI_BF16>(a, b, cm, args, grid, stream);
+            return args.a_gather ? launch<kModeFP8, MOE_EPI_SWIGLU_FP8, true>(a, b, cm, args, grid, stream)
+                                 : launch<kModeFP8, MOE_EPI_SWIGLU_FP8>(a, b, cm, args, grid, stream);
+        if (args.epilogue == MOE_EPI_BF16)
+            return args.a_gather ? launch<kModeFP8, MOE_EPI_BF16, true>(a, b, cm, args, grid, stream)
+                                 : launch<kModeFP8, MOE_EPI_BF16>(a, b, cm, args, grid, stream);
         return cudaErrorInvalidValue;
     }
     if (args.epilogue == MOE_EPI_SWIGLU_BF16) return launch<kModeBF16, MOE_EPI_SWIGLU_BF16>(a, b, cm, args, grid, stream);

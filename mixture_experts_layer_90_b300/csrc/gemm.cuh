@@ -35,6 +35,13 @@ struct GemmArgs {
     void* C;
     float* c_scales;     // MOE_EPI_SWIGLU_FP8: [Nd/256][M_total]
     uint16_t* h_out;     // MOE_EPI_SWIGLU_FP8, optional: the fp32 products rounded to bf16 [M_total][Nd]
+    // FP8, optional: A's rows gathered from a_src [a_rows][Kd]: row r of the grouped A
+    // is row a_gather[r] of it (r < a_gather_tk) or row r - a_gather_tk (the shared
+    // expert's rows); sa then has one column per row of a_src (lda_s = a_rows).
+    // nullptr: A is read through its tensor map as it stands.
+    const int32_t* a_gather;
+    int64_t a_gather_tk;
+    const uint8_t* a_src;
 };
 
 bool make_kmajor_map(CUtensorMap* tm, const void* base, bool bf16, uint64_t inner, uint64_t rows,

@@ -309,7 +309,7 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
                                                              perm_token, dest_row);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    {
+    if (x_perm) {   // null: the rows are not moved (the grouped GEMM gathers them)
         const int64_t R = T * K + (with_shared ? T : 0);
         int64_t blocks = (T + 7) / 8;
         if (blocks > cap * 2) blocks = cap * 2;

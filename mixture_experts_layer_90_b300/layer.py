@@ -22,7 +22,7 @@ import ctypes
 
 import torch
 
-from . import (MOE_DTYPE_BF16, MOE_DTYPE_F32, TRAIN_BUFFERS, LayerGrads, LayerMasters, LayerOutputs, LayerWeights,
+from . import (MOE_DISPATCH_GATHER, MOE_DISPATCH_SCATTER, MOE_DTYPE_BF16, MOE_DTYPE_F32, TRAIN_BUFFERS, LayerGrads, LayerMasters, LayerOutputs, LayerWeights,
                LayerWeightsT, _check, _p, _require_cuda, _stream, fp8_quant_128x128, fp8_transpose_128x128,
                load_library, moe_route_prepare_centroids)
 
@@ -35,7 +35,9 @@ def interleave_gate_up(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
 
 class MoELayer:
     def __init__(self, d, N, K, I, centroids, bias, w13, w2, w13_scales=None, w2_scales=None, n_groups=1,
-                 topk_groups=1, gamma=1e-3):
+                 topk_groups=1, gamma=1e-3, dispatch="scatter"):
+        """dispatch (FP8 layers): "scatter" (the permutation writes the grouped rows) or
+        "gather" (GEMM 1 gathers the quantised tokens by perm_token); the same bits."""
         _require_cuda()
         self.d, self.N, self.K, self.I = d, N, K, I
         self.n_groups, self.topk_groups, self.gamma = n_groups, topk_groups, gamma
@@ -51,7 +53,8 @@ class MoELayer:
             bias=bias.data_ptr(), w13=w13.data_ptr(),
             w13_scales=w13_scales.data_ptr() if w13_scales is not None else None,
             w2=w2.data_ptr(), w2_scales=w2_scales.data_ptr() if w2_scales is not None else None,
-            centroids_prepared=self.centroids_prepared.data_ptr())
+            centroids_prepared=self.centroids_prepared.data_ptr(),
+            dispatch={"scatter": MOE_DISPATCH_SCATTER, "gather": MOE_DISPATCH_GATHER}[dispatch])
         self._ws = {}
         self.loads = torch.zeros((N,), dtype=torch.int32, device=centroids.device)
 

@@ -233,6 +233,13 @@ def test_training_entry_points_check_their_arguments(L):
     wi = _layer_desc(I=384)
     assert L.moe_layer_forward_train(ctypes.byref(wi), p, T, p, ctypes.byref(outs), 1, p, 1 << 40, s) \
         == M.MOE_ERR_INVALID_ARG
+    # a dispatch mode that does not exist
+    wd = _layer_desc()
+    wd.dispatch = 7
+    assert L.moe_layer_forward(ctypes.byref(wd), p, T, p, ctypes.byref(outs), 1, p, 1 << 40, s) \
+        == M.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_forward_train(ctypes.byref(wd), p, T, p, ctypes.byref(outs), 1, p, 1 << 40, s) \
+        == M.MOE_ERR_INVALID_ARG
     # a too-small workspace
     assert L.moe_layer_forward_train(ctypes.byref(w), p, T, p, ctypes.byref(outs), 1, p, tr - 1, s) \
         == M.MOE_ERR_WORKSPACE

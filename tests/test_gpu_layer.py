@@ -172,3 +172,53 @@ def test_layer_graph_replay_matches_eager(fp8):
         assert torch.equal(graphed.loads, eager.loads)
         assert torch.equal(graphed.bias, eager.bias)
     assert _lib().device_status() == 0
+
+
+@pytest.mark.parametrize("sh", [S.LayerShape(T=301, d=512, N=32, K=4, I=256, name="dispatch-ragged"),
+                                S.LayerShape(T=96, d=512, N=64, K=6, I=256, n_groups=8, topk_groups=3,
+                                             name="dispatch-groups"),
+                                S.LayerShape(T=1, d=256, N=8, K=2, I=128, name="dispatch-one-token")])
+def test_layer_gather_and_scatter_dispatch_agree(sh):
+    """GEMM 1 gathering the quantised tokens by perm_token and the permutation
+    writing the grouped rows (the default) give the same bits: h', the routing,
+    the loads and the bias after an update."""
+    m = _lib()
+    layer = _build(sh)
+    b0 = layer.bias.clone()
+    u = S.tokens(sh).cuda()
+    res = {}
+    for mode in (m.MOE_DISPATCH_GATHER, m.MOE_DISPATCH_SCATTER):
+        layer.bias.copy_(b0)
+        layer._desc.dispatch = mode
+        idx = torch.empty((sh.T, sh.K), dtype=torch.int32, device="cuda")
+        gates = torch.empty((sh.T, sh.K), dtype=torch.float32, device="cuda")
+        out = layer.forward(u, topk_idx=idx, gates=gates, update_bias=True)
+        res[mode] = (out.clone(), idx, gates, layer.loads.clone(), layer.bias.clone())
+        assert m.device_status() == 0
+    for a, b in zip(res[m.MOE_DISPATCH_GATHER], res[m.MOE_DISPATCH_SCATTER]):
+        assert torch.equal(_bits(a), _bits(b))
+
+
+def _bits(t):
+    return t.view(torch.int32) if t.dtype == torch.float32 else t.view(torch.int16) if t.dtype == torch.bfloat16 \
+        else t
+
+
+def test_training_backward_same_under_both_dispatches():
+    """The training forward keeps GEMM 1's products for the backward; with the
+    gathered dispatch they, and so every gradient, are the scattered one's bits."""
+    m = _lib()
+    sh = S.LayerShape(T=300, d=256, N=8, K=2, I=256, name="dispatch-train")
+    layer = m.MoELayer.build(sh.d, sh.N, sh.K, sh.I, S.centroids(sh).cuda(), S.bias(sh).cuda(),
+                             lambda e: S.expert_weights(sh, e, device="cuda"), fp8=True, train=True, gamma=sh.gamma)
+    u = S.tokens(sh, seed=3).cuda()
+    G = S.grad_out(sh, seed=4).cuda()
+    res = {}
+    for mode in (m.MOE_DISPATCH_GATHER, m.MOE_DISPATCH_SCATTER):
+        layer._desc.dispatch = mode
+        out = layer.forward_train(u, update_bias=False)
+        du = layer.backward(u, G)
+        res[mode] = [out.clone(), du.clone(), layer.dw13.clone(), layer.dw2.clone(), layer.dcentroids.clone()]
+        assert m.device_status() == 0
+    for a, b in zip(res[m.MOE_DISPATCH_GATHER], res[m.MOE_DISPATCH_SCATTER]):
+        assert torch.equal(_bits(a), _bits(b))

@@ -56,3 +56,22 @@ def test_layer_v3_decode_group_limited(which):
     sh = S.DECODE_V3[which]
     tau, n_diff = _run_and_check(sh, zipf=True, u_seed=3)
     print(f"{sh.name}: achieved tau {tau:.3e}")
+
+
+def test_layer_v3_gather_and_scatter_dispatch_agree():
+    """At the V3 shape (Zipf-skewed groups, ragged tails), GEMM 1 gathering the
+    quantised tokens and the permutation writing the grouped rows give the same
+    h' bits."""
+    import mixture_experts_layer_90_b300 as m
+    from test_gpu_layer import _build
+    sh = S.LAYER_V3
+    layer = _build(sh, zipf=True)
+    u = S.tokens(sh, seed=1).cuda()
+    outs = {}
+    for mode in (m.MOE_DISPATCH_GATHER, m.MOE_DISPATCH_SCATTER):
+        layer._desc.dispatch = mode
+        outs[mode] = layer.forward(u, update_bias=False).clone()
+        assert m.device_status() == 0
+    assert torch.equal(outs[m.MOE_DISPATCH_GATHER].view(torch.int16), outs[m.MOE_DISPATCH_SCATTER].view(torch.int16))
+    del layer
+    torch.cuda.empty_cache()
