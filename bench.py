@@ -573,7 +573,7 @@ def case_route(moe, S, dev, args, flush, cpu_baseline=True):
     """Routing + dispatch at T=16384, d=7168, 256 fp32 centroids, top-8: gate
     logits, affinities, biased top-8, gates, loads (routing from centroids
     prepared once), the stable counting sort and scatter of bf16 rows, and the
-    bias update. HBM bound."""
+    bias update. The gate is a contraction, the rest moves bytes."""
     import numpy as np
 
     import oracle
@@ -619,6 +619,13 @@ def case_route(moe, S, dev, args, flush, cpu_baseline=True):
                         "frac": alg / ms / 1e6 / pk["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
                         "peak_source": f"{src} hbm copy"},
            "l2": "flushed before each step"}
+    # the gate is a contraction (three bf16 terms of the fp32 centroids), the rest moves bytes:
+    # the workload's floor is the gate at the bf16 peak plus the bytes at the HBM peak, in sequence
+    gate_flop = 2.0 * T * ((N + 255) // 256 * 256) * 3 * d
+    floor_ms = gate_flop / pk["bf16_tflops"] / 1e9 + alg / pk["hbm_gbs"] / 1e6
+    res["roofline_combined"] = {"bound": "tensor (gate) + hbm (the rest), in sequence", "floor_ms": floor_ms,
+                                "frac": floor_ms / ms, "gate_flop": gate_flop,
+                                "peak_source": f"{src} bf16 burst and hbm copy"}
     if cpu_baseline:
         n = 512
         uc, ec, bc = u[:n].cpu(), cent.cpu(), bias.cpu()
