@@ -2,8 +2,10 @@
 //
 // Combine (nlp-lineage.vercel.app "DeepSeek-V3 Technical Report (2024)", "The
 // notation"): h'_t = u_t + y_shared_t + sum_k g_{t,k} y_{dest_row[t,k]},
-// accumulated in fp32 in that order, stored as bf16. One warp per token, 16-byte
-// loads of every row it reads; HBM bound ((K + 3) rows of traffic per token).
+// accumulated in fp32 in that order, stored as bf16. One warp per (token, 256
+// columns), 16-byte loads of every row it reads; HBM bound ((K + 3) rows of
+// traffic per token). Small batches (decode) still give every SM work: a warp
+// per token walking its columns left 8 SMs busy at T = 64, bound by load latency.
 //
 // Bias update (learn.ifs.name summary, bias paragraph): after the step an
 // overloaded expert's bias falls by gamma and an underloaded one's rises;
@@ -20,7 +22,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const int32_t* __restrict__ dest_row, int64_t T, int d, int K,
                                                       int64_t R, uint16_t* __restrict__ out) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int64_t t = int64_t(blockIdx.x) * 8 + w; t < T; t += int64_t(gridDim.x) * 8) {
+    const int chunks = (d + 255) / 256;
+    const int64_t items = T * chunks;
+    for (int64_t item = int64_t(blockIdx.x) * 8 + w; item < items; item += int64_t(gridDim.x) * 8) {
+        const int64_t t = item / chunks;
+        const int c0 = int(item - t * chunks) * 256;
         int my_row = 0;
         float my_g = 0.0f;
         if (lane < K) {
@@ -32,7 +38,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                 my_g = 0.0f;
             }
         }
-        for (int c0 = 0; c0 < d; c0 += 256) {
+        {
             const int c = c0 + lane * 8;
             const bool active = c < d;
             float acc[8];
@@ -96,7 +102,7 @@ cudaError_t launch_combine(const uint16_t* u, const uint16_t* y_shared, const ui
                            const int32_t* dest_row, int64_t T, int d, int K, int64_t R, uint16_t* out,
                            cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    int64_t blocks = (T + 7) / 8;
+    int64_t blocks = (T * ((d + 255) / 256) + 7) / 8;   // a warp per (token, 256 columns)
     const int64_t cap = int64_t(num_sms()) * 16;
     if (blocks > cap) blocks = cap;
     combine_kernel<<<int(blocks), 256, 0, stream>>>(u, y_shared, y_perm, gates, dest_row, T, d, K, R, out);

@@ -11,9 +11,9 @@
 //   small   batches of at most 8192 pairs over at most 256 experts: count,
 //           scan and rank in one block (one launch instead of three; the
 //           decode and small layers are bound by dependent launches)
-//   scatter warp per token: the token's row is read once and written to its K
-//           rows (and to the shared expert's row), optionally quantised to
-//           E4M3 per 1x128 tile on the way.
+//   scatter warp per (token, 512 columns): the piece is read once and written
+//           to the token's K rows (and to the shared expert's row), optionally
+//           quantised to E4M3 per 1x128 tile on the way.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -198,13 +198,13 @@ __global__ void __launch_bounds__(1024) perm_small_kernel(const int32_t* __restr
 }
 
 // Token-major scatter of rows (bf16 copy or E4M3 1x128 quantisation). A warp
-// owns one token and moves 512 columns per step, 16 per lane:
+// takes one (token, 512 columns) item, 16 columns per lane (a warp per token
+// walking its columns left most SMs idle in decode batches):
 //   E4M3: lane l takes columns 16l..16l+15, so a 128-element tile sits in 8
 //         lanes and each destination row gets one 16-byte store per lane
 //         (512 contiguous bytes per warp);
 //   bf16: lane l takes columns 8l..8l+7 and 256+8l..256+8l+7, so each of
 //         the two 16-byte stores per destination covers 512 contiguous bytes.
-// The next step's columns are loaded while this step's are written.
 template <bool kFP8>
 __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint16_t* __restrict__ x, int64_t T, int d, int K,
                                                            const int32_t* __restrict__ dest_row, int with_shared,
@@ -215,20 +215,21 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(const uint16_t* __res
     const int off_a = kFP8 ? lane * 16 : lane * 8;    // columns of the lane's two 8-element pieces
     const int off_b = kFP8 ? lane * 16 + 8 : 256 + lane * 8;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int64_t t = int64_t(blockIdx.x) * 8 + w; t < T; t += int64_t(gridDim.x) * 8) {
+    const int steps = (d + 511) / 512;
+    const int64_t items = T * steps;
+    for (int64_t item = int64_t(blockIdx.x) * 8 + w; item < items; item += int64_t(gridDim.x) * 8) {
+        const int64_t t = item / steps;
+        const int c0 = int(item - t * steps) * 512;
         int my_dest = 0;
         if (lane < K) my_dest = __ldg(dest_row + t * K + lane);
         else if (lane == K && with_shared) my_dest = int(int64_t(T) * K + t);
         const uint16_t* src = x + t * d;
-        uint4 n0 = off_a < d ? __ldg(reinterpret_cast<const uint4*>(src + off_a)) : zero;
-        uint4 n1 = off_b < d ? __ldg(reinterpret_cast<const uint4*>(src + off_b)) : zero;
-        for (int c0 = 0; c0 < d; c0 += 512) {
+        {
             const int ca = c0 + off_a, cb = c0 + off_b;
             // d is a multiple of 128: the 8 lanes of an E4M3 tile are all active or all idle
             const bool act_a = ca < d, act_b = cb < d;
-            const uint4 v0 = n0, v1 = n1;
-            if (ca + 512 < d) n0 = __ldg(reinterpret_cast<const uint4*>(src + ca + 512));
-            if (cb + 512 < d) n1 = __ldg(reinterpret_cast<const uint4*>(src + cb + 512));
+            const uint4 v0 = act_a ? __ldg(reinterpret_cast<const uint4*>(src + ca)) : zero;
+            const uint4 v1 = act_b ? __ldg(reinterpret_cast<const uint4*>(src + cb)) : zero;
             if constexpr (!kFP8) {
                 for (int k = 0; k < n_dest; ++k) {
                     const int row = __shfl_sync(0xffffffffu, my_dest, k);
@@ -311,7 +312,7 @@ cudaError_t launch_permute(const uint16_t* x, int64_t T, int d, const int32_t* t
     }
     if (x_perm) {   // null: the rows are not moved (the grouped GEMM gathers them)
         const int64_t R = T * K + (with_shared ? T : 0);
-        int64_t blocks = (T + 7) / 8;
+        int64_t blocks = (T * ((d + 511) / 512) + 7) / 8;   // a warp per (token, 512 columns)
         if (blocks > cap * 2) blocks = cap * 2;
         if (out_dtype == MOE_DTYPE_E4M3)
             perm_scatter_kernel<true><<<int(blocks), 256, 0, stream>>>(x, T, d, K, dest_row, with_shared, x_perm,

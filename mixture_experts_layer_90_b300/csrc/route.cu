@@ -96,17 +96,24 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
         // bit j: expert 32j + lane is out of the running (past N, outside the kept
         // groups, or already chosen)
         uint32_t excl = 0;
+        // z of each of the lane's experts: the split-K partials added in split order;
+        // a split's J loads are issued together (small batches take many splits)
+        float zj[J];
+        const float* zt = zpart + t * n_pad + lane;
+#pragma unroll
+        for (int j = 0; j < J; ++j) zj[j] = 32 * j + lane < N ? __ldg(zt + 32 * j) : 0.0f;
+        for (int p = 1; p < splits; ++p) {
+            float v[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) v[j] = 32 * j + lane < N ? __ldg(zt + p * plane + 32 * j) : 0.0f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) zj[j] += v[j];
+        }
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int i = 32 * j + lane;
-            float z = 0.0f;
-            if (i < N) {
-                const float* zp = zpart + t * n_pad + i;
-                z = __ldg(zp);
-                for (int p = 1; p < splits; ++p) z += __ldg(zp + p * plane);
-            } else {
-                excl |= 1u << j;
-            }
+            const float z = zj[j];
+            if (i >= N) excl |= 1u << j;
             s[j] = __fdiv_rn(1.0f, 1.0f + expf(-z));
             const float kv = s[j] + b[j];
             // a NaN key (NaN token or bias) ranks below every number: it can still be
