@@ -690,14 +690,18 @@ def case_decode(moe, S, dev, args, flush, v3_layer, dsh, cpu_baseline=True):
     u = S.tokens(dsh, seed=3, device=dev)
     out = torch.empty_like(u)
     ms_eager = time_launches(lambda: layer.forward(u, out, update_bias=False), args.steps, args.warmup, flush)
-    graph = layer.capture(u, out, update_bias=False)   # a decode step is replayed, not relaunched
-    ms = time_launches(graph.replay, args.steps, args.warmup, flush)
+    graph = layer.capture(u, out, update_bias=False)   # a decode step replayed, not relaunched
+    ms_graph = time_launches(graph.replay, args.steps, args.warmup, flush)
+    # both ways of running a decode step are timed; the faster one is the entry's time
+    ms = min(ms_graph, ms_eager)
+    how = "CUDA-graph replay" if ms_graph <= ms_eager else "eager call"
     active = int((layer.loads > 0).sum().item()) + 1
     per_expert = 3 * dsh.I * dsh.d + 4 * (3 * dsh.I * dsh.d // 16384)
     alg = active * per_expert + 2 * dsh.T * dsh.d * 2
     pk, src = peaks()
-    res = {"workload": dsh.name, "ms": ms, "ms_eager": ms_eager, "tokens_per_s": dsh.T / ms * 1e3,
-           "active_experts": active, "timing": "CUDA-graph replay of the layer call (eager call beside it)",
+    res = {"workload": dsh.name, "ms": ms, "ms_graph": ms_graph, "ms_eager": ms_eager, "tokens_per_s": dsh.T / ms * 1e3,
+           "active_experts": active,
+           "timing": f"the faster of a CUDA-graph replay and an eager call of the layer: {how}",
            "roofline": {"bound": "hbm", "achieved": alg / ms / 1e6, "peak": pk["hbm_gbs"], "unit": "GB/s",
                         "frac": alg / ms / 1e6 / pk["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
                         "peak_source": f"{src} hbm copy"},
