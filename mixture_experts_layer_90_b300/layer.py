@@ -39,6 +39,9 @@ class MoELayer:
         """dispatch (FP8 layers): "scatter" (the permutation writes the grouped rows) or
         "gather" (GEMM 1 gathers the quantised tokens by perm_token); the same bits."""
         _require_cuda()
+        modes = {"scatter": MOE_DISPATCH_SCATTER, "gather": MOE_DISPATCH_GATHER}
+        if dispatch not in modes:
+            raise ValueError(f"dispatch must be one of {sorted(modes)}, not {dispatch!r}")
         self.d, self.N, self.K, self.I = d, N, K, I
         self.n_groups, self.topk_groups, self.gamma = n_groups, topk_groups, gamma
         self.fp8 = w13.dtype == torch.uint8
@@ -54,7 +57,7 @@ class MoELayer:
             w13_scales=w13_scales.data_ptr() if w13_scales is not None else None,
             w2=w2.data_ptr(), w2_scales=w2_scales.data_ptr() if w2_scales is not None else None,
             centroids_prepared=self.centroids_prepared.data_ptr(),
-            dispatch={"scatter": MOE_DISPATCH_SCATTER, "gather": MOE_DISPATCH_GATHER}[dispatch])
+            dispatch=modes[dispatch])
         self._ws = {}
         self.loads = torch.zeros((N,), dtype=torch.int32, device=centroids.device)
 
